@@ -1,0 +1,347 @@
+"""Benchmark of the fused attention forward on GB300, one JSON line on stdout (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload s4k|s8k|s16k|ragged]
+  python bench.py --impl reference ...      # the CPU oracle on the host cores, same metric
+
+A step is one attn_fwd call (the whole hot path: one kernel) on one batch of seeded
+synthetic BF16 input already resident in HBM. Between timed steps L2 is flushed by writing a
+256 MB buffer; each step is timed by its own CUDA events on the launching stream, so the
+flush is outside the measured kernel time. Under torchrun every rank runs the same workload
+on its own GPU (independent replicas, no collective on the data path: weak scaling); the
+value is all ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (4·B·H·S²·D) at S=4K/8K/16K; % of GB300 BF16 dense peak"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
+# valid only for the kernel source it was taken on (hash of the CUDA sources).
+TRAFFIC = {}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_attention_forward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")) and name != "selftest.cu":
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def time_oracle(w: wl.Workload, q, k, v, budget_s: float, min_chunks: int = 1):
+    """Time the oracle on row chunks (all heads) until `budget_s` has elapsed. Returns
+    (TFLOPS, seconds, rows_per_head, cores)."""
+    from oracle import attn_ref as ref
+    qf, kf, vf = wl.to_f64(q), wl.to_f64(k), wl.to_f64(v)
+    chunk = 32
+    rows_done = 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        r0 = (i * chunk) % w.S
+        rows = list(range(r0, min(w.S, r0 + chunk)))
+        ref.attention_rows(qf, kf, vf, w.scale, rows)
+        rows_done += len(rows)
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and i >= min_chunks:
+            break
+    flops = 4.0 * w.B * w.H * rows_done * w.S * w.D
+    return flops / el / 1e12, el, rows_done, os.cpu_count()
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v = wl.make_qkv(w)
+    warm = max(args.warmup, 3)
+    for _ in range(warm):
+        time_oracle(w, q, k, v, budget_s=0.0)
+    rates, secs, rows = [], 0.0, 0
+    for _ in range(args.steps):
+        r, el, nrows, cores = time_oracle(w, q, k, v, budget_s=args.ref_step_seconds)
+        rates.append(r)
+        secs += el
+        rows += nrows
+    value = statistics.median(rates)
+    sample = (f"{args.steps} steps; each step times the fp64 oracle on >= {args.ref_step_seconds:g} s "
+              f"of 32-query-row chunks over all {w.B * w.H} heads ({rows} rows per head in total) "
+              f"of {w.label()}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": warm, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.label(), "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": False},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_gpu(attn, torch, w, q, k, v, o, lse, steps, warmup, flush, stream):
+    for _ in range(warmup):
+        attn.fwd(q, k, v, w.scale, out=o, lse=lse)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.add_(1)  # write > L2 between timed calls
+        starts[i].record(stream)
+        attn.fwd(q, k, v, w.scale, out=o, lse=lse)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_gpu(args, w):
+    import torch
+    import dense_attention_forward_gb300 as attn
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = (t.to(dev) for t in wl.make_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    warm = max(args.warmup, 3)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    barrier()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        times = time_gpu(attn, torch, w, q, k, v, o, lse, args.steps, warm, flush, stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    kern_ms = sum(times) / len(times)
+    if dist is not None:
+        t = torch.tensor([kern_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kern_ms = float(t.item())
+    value = world * w.flops / (kern_ms * 1e-3) / 1e12
+    status = attn.device_status(reset=True)
+
+    # ---- end to end: pinned host -> device, attn_fwd, device -> pinned host, every step
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        od, ld = attn.fwd(qd, kd, vd, w.scale)
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(ld, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    # ---- other workloads of the same metric (single GPU, same method, fewer steps)
+    sweep = {}
+    if not args.no_sweep:
+        for name in args.sweep:
+            if name == w.name:
+                continue
+            ws = wl.ALL[name]
+            qs, ks, vs = (t.to(dev) for t in wl.make_qkv(ws))
+            os_, ls_ = torch.empty_like(qs), torch.empty((ws.B, ws.H, ws.S), device=dev)
+            ts = time_gpu(attn, torch, ws, qs, ks, vs, os_, ls_, args.sweep_steps, 3, flush, stream)
+            ms = sum(ts) / len(ts)
+            sweep[name] = {"workload": ws.label(), "ms": round(ms, 4),
+                           "tflops": round(ws.flops / (ms * 1e-3) / 1e12, 1)}
+            del qs, ks, vs, os_, ls_
+        status |= attn.device_status(reset=True)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops / (kern_ms * 1e-3) / 1e12  # per GPU, per launch
+    trec = TRAFFIC.get(w.name)
+    traffic = trec[0] if (trec and trec[1] == source_hash()) else None
+    for name, rec in sweep.items():
+        rec["frac_of_peak"] = round(rec["tflops"] / peak, 4)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": warm, "ms_per_step": round(kern_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.label(), "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                   "causal": False, "scale": w.scale, "inputs": "seeded N(0,1) BF16",
+                   "l2": "flushed between timed steps (256 MB write); inputs 268 MB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peaks_src} bf16_tflops (burst, cuBLAS 8192^3)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+        "device_status": status,
+        "sweep": sweep,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        qc, kc, vc = wl.make_qkv(w)
+        rate, el, rows, cores = time_oracle(w, qc, kc, vc, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle on {rows} query rows of each of the {w.B * w.H} heads of "
+                      f"{w.label()} ({el:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="s4k", choices=sorted(wl.ALL))
+    ap.add_argument("--sweep", nargs="*", default=["s8k", "s16k", "ragged"])
+    ap.add_argument("--sweep-steps", type=int, default=100)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args()
+    w = wl.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,68 @@
+"""GB300 (sm_103a) fused dense attention forward: O = softmax(scale * Q K^T) V and lse.
+
+Python face of the C ABI in include/attn.h. Only argument checking and marshalling happen
+here; every step of the computation runs in the CUDA kernel of libattn.so. PyTorch provides
+device memory and the current stream.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import AttnError, attn_fwd, device_status, lib  # noqa: F401
+
+__all__ = ["fwd", "attn_fwd", "device_status", "AttnError", "lib"]
+
+
+def _check(name, t, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, S, D]")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, S, D]")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True,
+        stream=None):
+    """Attention forward on the current CUDA stream (or `stream`).
+
+    q, k, v: bfloat16 CUDA tensors, contiguous [B, H, S, 128]. scale defaults to 1/sqrt(128).
+    Returns (o, lse) with o bfloat16 [B, H, S, 128] and lse float32 [B, H, S] (natural log),
+    or (o, None) when return_lse is False. `out` / `lse` may be given preallocated.
+    """
+    import torch
+    _check("q", q)
+    B, H, S, D = q.shape
+    _check("k", k, q.shape)
+    _check("v", v, q.shape)
+    if q.device != k.device or q.device != v.device:
+        raise ValueError("q, k, v must be on the same device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check("out", out, q.shape)
+    if return_lse:
+        if lse is None:
+            lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+        elif lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, S):
+            raise ValueError("lse must be a contiguous float32 [B, H, S] tensor")
+    else:
+        lse = None
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, S, D, float(scale),
+                      stream.cuda_stream)
+    if st != 0:
+        raise AttnError(st)
+    return out, lse

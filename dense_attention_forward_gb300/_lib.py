@@ -1,0 +1,80 @@
+"""ctypes binding of include/attn.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+SELFTEST_PATH = os.path.join(PKG, "libattn_selftest.so")
+
+ATTN_OK = 0
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED_DIM",
+    3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_UNSUPPORTED_DEVICE", 5: "ATTN_ERR_LAUNCH",
+    6: "ATTN_ERR_TIMEOUT",
+}
+
+# Every symbol include/attn.h declares, with its ctypes signature.
+SIGNATURES = {
+    "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
+    "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
+    "attn_version": (ctypes.c_int, []),
+}
+
+_lib = None
+_selftest = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = "attn_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {STATUS_NAMES.get(status, status)} "
+                         f"({lib().attn_status_string(status).decode()})")
+
+
+def lib():
+    """The loaded libattn.so. Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first (python -m dense_attention_forward_gb300.build "
+                "or __graft_entry__.build()); the attention path has no CPU fallback")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def selftest_lib():
+    global _selftest
+    if _selftest is None:
+        if not os.path.exists(SELFTEST_PATH):
+            raise RuntimeError(f"{SELFTEST_PATH} is missing: build it first")
+        h = ctypes.CDLL(SELFTEST_PATH)
+        h.attn_selftest_gemm.restype = ctypes.c_int
+        h.attn_selftest_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int, ctypes.c_void_p]
+        _selftest = h
+    return _selftest
+
+
+def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None, B: int, H: int,
+             S: int, D: int, scale: float, stream: int | None) -> int:
+    """Direct call of the C entry point with raw addresses; returns the status code."""
+    return lib().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, S, D, scale, stream)
+
+
+def device_status(reset: bool = True) -> int:
+    word = ctypes.c_uint(0)
+    st = lib().attn_device_status(ctypes.byref(word), 1 if reset else 0)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_device_status")
+    return word.value

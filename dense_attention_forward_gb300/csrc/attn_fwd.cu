@@ -1,0 +1,633 @@
+// attn_fwd.cu -- fused dense attention forward for GB300 (sm_103a): kernel + C ABI.
+//
+// O = softmax(scale * Q K^T) V and the fp32 logsumexp for BF16 Q/K/V of shape [B, H, S, 128].
+//
+// Design (after "B200 attention kernel from scratch to ~SOTA in 60 figures (CUDA/PTX)",
+// cited as [B200-attn]; its kernels were written for B200 and are prior art here):
+//  * Work split (Ch. 1 §ii, Ch. 5): one CTA owns two consecutive 128-row Q tiles of one
+//    (batch, head) and walks every 128-key K/V tile of that head; each K/V tile loaded into
+//    shared memory serves both Q tiles.
+//  * Loads (Ch. 3, Ch. 6): one TMA warp streams K and V as separate tokens through a
+//    kStages-slot ring of 32 KB SW128 slots; a slot is refilled once its last consumer (the
+//    second Q tile's QK for K, its PV for V) has committed.
+//  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 7): one elected thread issues tcgen05.mma M128 N128 K16:
+//    S_q = Q_q K^T (both K-major SW128 in shared memory) and O_q += P_q V (P from tensor
+//    memory, V MN-major SW128). The steady state issues PqV(i) then QqK(i+1).
+//  * Softmax (Ch. 1 §B, Ch. 8, Ch. 11): 4 warps per Q tile, one thread per row, the whole
+//    128-score row in registers; base-2 exponent with scale*log2(e) folded into one factor,
+//    row max taken on raw scores; the kept row max moves only when the tile max exceeds it
+//    by >= 8 (base 2); P is packed to BF16 pairs and stored over S in tensor memory. O is
+//    normalised by the sum of the BF16-rounded P that PV consumes; lse uses the fp32 sum.
+//  * Correction (Ch. 11, Ch. 12): 4 warps shared by both Q tiles rescale O in tensor memory
+//    when any row of their 32 rebased, then run the epilogue (O / l -> BF16 -> SW128 shared
+//    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
+//
+// TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
+// the first 64 columns of S_q. Every mbarrier wait is bounded (about two seconds); a CTA that
+// gives up records the failure in a device status word, drains its own TMA loads and MMAs,
+// frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int kBlock = 128;                      // rows per Q tile and keys per K/V tile
+constexpr int kHeadDim = 128;                    // D
+constexpr int kTileBytes = kBlock * kHeadDim * 2;  // one 128x128 BF16 tile: 32 KB
+constexpr int kSliceBytes = kBlock * 128;        // 128 rows x 128 B: one SW128 column of atoms
+constexpr int kStages = 3;                       // K/V ring slots
+constexpr int kThreads = 512;                    // 16 warps
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr float kRebaseLog2 = 8.0f;              // Ch. 11 threshold, base-2 units
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr int kOffQ = 0;                                   // Q0, Q1 (later: O staging)
+constexpr int kOffKV = kOffQ + 2 * kTileBytes;             // K/V ring
+constexpr int kOffBar = kOffKV + kStages * kTileBytes;     // mbarriers
+// barrier indices
+constexpr int kBarQFull = 0;                     // [2]
+constexpr int kBarKVFull = 2;                    // [kStages]
+constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages]
+constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_q in TMEM (MMA commit)
+constexpr int kBarPFull = kBarSFull + 2;           // [2] P_q in TMEM (128 softmax threads)
+constexpr int kBarOSafe = kBarPFull + 2;           // [2] O_q rescaled or untouched (128 correction threads)
+constexpr int kBarOFull = kBarOSafe + 2;           // [2] PV_q done (MMA commit)
+constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (128)
+constexpr int kBarLReady = kBarStats + 2;          // [2] final row sums published (128)
+constexpr int kBarMmaDone = kBarLReady + 2;        // [1] drain after a failure
+constexpr int kNumBars = kBarMmaDone + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kOffAlpha = (kOffAbort + 4 + 15) & ~15;      // float[2][128]
+constexpr int kOffLFinal = kOffAlpha + 2 * kBlock * 4;     // float[2][128]
+constexpr int kSmemUsed = kOffLFinal + 2 * kBlock * 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for the 1024-byte alignment
+
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffKV % 1024 == 0 && kTileBytes % 1024 == 0, "SW128 atoms need 1024-B alignment");
+
+// Failure codes written to the device status word: 0xA77E0000 | role << 8 | barrier index.
+enum : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleCorrection = 4 };
+
+__device__ unsigned int g_attn_status = 0;
+
+struct Params {
+  float* lse;
+  int S;            // sequence length
+  int n_kv;         // ceil(S / 128)
+  int n_qp;         // ceil(S / 256): CTAs per (b, h)
+  float scale_log2; // scale * log2(e)
+};
+
+struct Ctl {
+  uint32_t bar0;                  // smem address of barrier 0
+  volatile uint32_t* abort_flag;  // shared
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+};
+
+__device__ __forceinline__ bool wait_slow(const Ctl& c, int b, uint32_t parity, uint32_t role,
+                                       bool watch_abort, uint64_t limit_ns) {
+  const uint32_t bar = c.bar(b);
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (watch_abort && *c.abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        if (watch_abort) {
+          *c.abort_flag = 1u;
+          atomicCAS(&g_attn_status, 0u, 0xA77E0000u | (role << 8) | static_cast<uint32_t>(b));
+        }
+        return false;
+      }
+    }
+  }
+}
+
+// Wait for phase `parity` of barrier b; false if this CTA is giving up.
+__device__ __forceinline__ bool wait_bar(const Ctl& c, int b, uint32_t parity, uint32_t role) {
+  if (mbar_try_wait(c.bar(b), parity)) return true;
+  return wait_slow(c, b, parity, role, true, kWaitLimitNs);
+}
+
+// Warp-uniform variant for code that continues with warp-collective tcgen05 instructions.
+__device__ __forceinline__ bool wait_bar_warp(const Ctl& c, int b, uint32_t parity, uint32_t role) {
+  const bool ok = wait_bar(c, b, parity, role);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qp = blockIdx.x % p.n_qp;
+  const int bh = blockIdx.x / p.n_qp;
+  const int q0 = qp * 2 * kBlock;
+  const int n = p.n_kv;
+
+  Ctl c;
+  c.bar0 = base + kOffBar;
+  c.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  float* const alpha_sm = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* const lfin_sm = reinterpret_cast<float*>(smem + kOffLFinal);
+  const uint32_t q_smem = base + kOffQ;
+  const uint32_t kv_smem = base + kOffKV;
+
+  if (threadIdx.x == 0) {
+    mbar_init(c.bar(kBarQFull + 0), 1);
+    mbar_init(c.bar(kBarQFull + 1), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(c.bar(kBarKVFull + s), 1);
+      mbar_init(c.bar(kBarKVEmpty + s), 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(c.bar(kBarSFull + q), 1);
+      mbar_init(c.bar(kBarPFull + q), 128);
+      mbar_init(c.bar(kBarOSafe + q), 128);
+      mbar_init(c.bar(kBarOFull + q), 1);
+      mbar_init(c.bar(kBarStats + q), 128);
+      mbar_init(c.bar(kBarLReady + q), 128);
+    }
+    mbar_init(c.bar(kBarMmaDone), 1);
+    *c.abort_flag = 0u;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + kOffTmemSlot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Register split (warpgroup granularity, set at the top of each role's branch so the
+  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 80 +
+  // load/MMA WG 48 = 65536 = 512 threads x 128 registers at launch.
+  if (warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;");
+  }
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
+      const uint64_t keep = l2_policy_evict_last();   // K/V: re-read by every CTA of the head
+      const uint64_t once = l2_policy_evict_first();  // Q: read once
+      bool ok = true;
+      int issued = 0;
+      for (int q = 0; q < 2 && ok; ++q) {
+        const uint32_t bar = c.bar(kBarQFull + q);
+        const uint32_t dst = q_smem + q * kTileBytes;
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        tma_load_3d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, bh, once);
+        tma_load_3d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, bh, once);
+      }
+      for (int t = 0; t < 2 * n; ++t) {
+        const int s = t % kStages;
+        const int use = t / kStages;
+        if (t >= kStages) {
+          if (!wait_bar(c, kBarKVEmpty + s, (use - 1) & 1, kRoleLoad)) { ok = false; break; }
+        }
+        const uint32_t bar = c.bar(kBarKVFull + s);
+        const uint32_t dst = kv_smem + s * kTileBytes;
+        const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+        const int row = (t >> 1) * kBlock;
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        tma_load_3d_hint(dst, map, bar, 0, row, bh, keep);
+        tma_load_3d_hint(dst + kSliceBytes, map, bar, 64, row, bh, keep);
+        issued = t + 1;
+      }
+      if (!ok) {
+        // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
+        for (int q = 0; q < 2; ++q) wait_slow(c, kBarQFull + q, 0, kRoleLoad, false, kDrainLimitNs);
+        for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
+          wait_slow(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleLoad, false, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
+      // Descriptors are built once; the start-address field (bits 0-13, 16-byte units) is
+      // advanced by plain addition, which never carries out of the field here (< 256 KB).
+      // K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
+      // MN-major SW128 (V): 8-row groups along K 1024 B apart (SBO), the two 64-wide halves
+      // of N 16 KB apart (LBO).
+      const uint64_t dq0 = smem_desc_sw128(q_smem, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(kv_smem, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
+      // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
+      // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further).
+      auto issue_qk = [&](int q, int slot) {
+        const uint64_t a = dq0 + static_cast<uint64_t>((q * kTileBytes) >> 4);
+        const uint64_t b = dk0 + static_cast<uint64_t>((slot * kTileBytes) >> 4);
+        const uint32_t d = tmem + static_cast<uint32_t>(q) * 128u;
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(d, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
+      // V rows [16kk, 16kk+16) (2048 B further per step).
+      auto issue_pv = [&](int q, int slot, bool first) {
+        const uint64_t b = dv0 + static_cast<uint64_t>((slot * kTileBytes) >> 4);
+        const uint32_t a = tmem + static_cast<uint32_t>(q) * 128u;
+        const uint32_t d = tmem + 256u + static_cast<uint32_t>(q) * 128u;
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_bf16_ts(d, a + kk * 8, b + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                      (first && kk == 0) ? 0u : 1u);
+        }
+      };
+      auto full_wait = [&](int t) {
+        return wait_bar(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleMma);
+      };
+      bool ok = true;
+      do {
+        // prologue: Q0 K0, Q1 K0
+        if (!wait_bar(c, kBarQFull + 0, 0, kRoleMma) || !full_wait(0)) { ok = false; break; }
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(c.bar(kBarSFull + 0));
+        if (!wait_bar(c, kBarQFull + 1, 0, kRoleMma)) { ok = false; break; }
+        tc_fence_after();
+        issue_qk(1, 0);
+        mma_commit(c.bar(kBarSFull + 1));
+        mma_commit(c.bar(kBarKVEmpty + 0));
+        for (int i = 0; i < n && ok; ++i) {
+          const int tv = 2 * i + 1;
+          if (!full_wait(tv)) { ok = false; break; }
+          for (int q = 0; q < 2; ++q) {
+            if (!wait_bar(c, kBarPFull + q, i & 1, kRoleMma)) { ok = false; break; }
+            if (i > 0 && !wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleMma)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(q, tv % kStages, i == 0);
+            mma_commit(c.bar(kBarOFull + q));
+            if (q == 1) mma_commit(c.bar(kBarKVEmpty + tv % kStages));
+            if (i + 1 < n) {
+              const int tk = 2 * (i + 1);
+              if (q == 0 && !full_wait(tk)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(q, tk % kStages);
+              mma_commit(c.bar(kBarSFull + q));
+              if (q == 1) mma_commit(c.bar(kBarKVEmpty + tk % kStages));
+            }
+          }
+        }
+      } while (false);
+      if (!ok) {
+        // Give up: make sure every MMA issued so far has finished before TMEM is freed.
+        mma_commit(c.bar(kBarMmaDone));
+        wait_slow(c, kBarMmaDone, 0, kRoleMma, false, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ softmax (Q tile q)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+    const int q = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
+    const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
+    const float sl2 = p.scale_log2;
+    const int rem = p.S - (n - 1) * kBlock;  // valid keys in the last tile, 1..128
+    float m_kept = -INFINITY;                 // kept row max, base-2 units
+    float l = 0.f;                            // running row sum of BF16 P (normalises O)
+    float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32_x128_sync(tS, sr);
+      float s[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sr[j]);
+      if (i == n - 1 && rem < kBlock) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) s[j] = (j < rem) ? s[j] : -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx[j] = s[j];
+#pragma unroll
+      for (int j = 8; j < 128; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+      const float tile_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+          sl2;
+      if (i == 0) {
+        m_kept = tile_max;
+      } else {
+        float alpha = 1.0f;
+        if (tile_max - m_kept >= kRebaseLog2) {
+          alpha = ex2_ftz(m_kept - tile_max);
+          l *= alpha;
+          lf *= alpha;
+          m_kept = tile_max;
+        }
+        alpha_sm[q * kBlock + row] = alpha;
+        mbar_arrive(c.bar(kBarStats + q));
+      }
+      const float neg_m = -m_kept;
+      float lb2[2] = {0.f, 0.f}, lf2[2] = {0.f, 0.f};
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const float p0 = ex2_ftz(fmaf(s[2 * j], sl2, neg_m));
+        const float p1 = ex2_ftz(fmaf(s[2 * j + 1], sl2, neg_m));
+        pk[j] = pack_bf16x2(p0, p1);
+        // Two row sums: lb adds the BF16-rounded P that the PV product consumes and
+        // normalises O (numerator and denominator carry the same weights; with the rebase
+        // threshold P reaches 256, where a fp32-vs-BF16 mismatch shows on rows dominated by
+        // one key); lf adds the fp32 P for the logsumexp.
+        lb2[j & 1] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+        lf2[j & 1] += p0 + p1;
+      }
+      l += lb2[0] + lb2[1];
+      lf += lf2[0] + lf2[1];
+      tmem_st32_x64(tS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(c.bar(kBarPFull + q));
+    }
+    if (ok) {
+      lfin_sm[q * kBlock + row] = l;
+      mbar_arrive(c.bar(kBarLReady + q));
+      const int grow = q0 + q * kBlock + row;
+      if (p.lse != nullptr && grow < p.S)
+        p.lse[static_cast<size_t>(bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------------------------ correction + epilogue
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
+    bool ok = true;
+    for (int i = 1; i < n && ok; ++i) {
+      for (int q = 0; q < 2; ++q) {
+        if (!wait_bar_warp(c, kBarStats + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
+        const float alpha = alpha_sm[q * kBlock + row];
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          if (!wait_bar_warp(c, kBarOFull + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32_x32_sync(tO[q] + cc * 32, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32_x32(tO[q] + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(c.bar(kBarOSafe + q));
+      }
+    }
+    // epilogue: O / l -> BF16 -> SW128 staging in the dead Q buffer -> TMA store
+    for (int q = 0; q < 2 && ok; ++q) {
+      if (!wait_bar_warp(c, kBarLReady + q, 0, kRoleCorrection)) { ok = false; break; }
+      if (!wait_bar_warp(c, kBarOFull + q, (n - 1) & 1, kRoleCorrection)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = 1.0f / lfin_sm[q * kBlock + row];
+      const uint32_t stage = q_smem + q * kTileBytes;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32_x32_sync(tO[q] + cc * 32, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int chunk = cc * 4 + t;  // 16-byte chunk of the 256-byte row, 0..15
+          const uint32_t addr = stage + (chunk >> 3) * kSliceBytes + row * 128 +
+                                (static_cast<uint32_t>((chunk & 7) ^ (row & 7)) << 4);
+          st_shared_v4(addr, pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (warp == 8 && lane == 0 && q0 + q * kBlock < p.S) {
+        tma_store_3d(&tm_o, stage, 0, q0 + q * kBlock, bh);
+        tma_store_3d(&tm_o, stage + kSliceBytes, 64, q0 + q * kBlock, bh);
+        tma_store_commit();
+      }
+    }
+    if (warp == 8 && lane == 0) tma_store_wait_read_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ==========================================================================================
+// Host side
+// ==========================================================================================
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported/failed
+std::mutex g_dev_mutex;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Checks the device once (compute capability 10.3) and sets the kernel's shared-memory limit.
+int prepare_device(int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return ATTN_ERR_UNSUPPORTED_DEVICE;
+  }
+  *dev_out = dev;
+  if (dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 1) return ATTN_OK;
+  if (st == -1) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st != 0) return st == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      major != 10 || minor != 3) {
+    cudaGetLastError();
+    g_dev_state[dev].store(-1, std::memory_order_release);
+    return ATTN_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  g_dev_state[dev].store(1, std::memory_order_release);
+  return ATTN_OK;
+}
+
+// [D, S, B*H] BF16 view of a contiguous [B, H, S, D] tensor; 64x128 boxes, 128-byte swizzle.
+bool encode_bhsd(CUtensorMap* map, const void* ptr, int S, long long BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                 static_cast<cuuint64_t>(S) * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, kBlock, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace gb300
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int S, int D, float scale, void* stream) {
+  using namespace gb300;
+  if (D != kHeadDim) return ATTN_ERR_UNSUPPORTED_DIM;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || S <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_qp = (static_cast<long long>(S) + 2 * kBlock - 1) / (2 * kBlock);
+  if (BH > (1ll << 31) - 1 || BH * n_qp > (1ll << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * S * kHeadDim * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * S * 4;
+  if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+      overlaps(o, tensor_bytes, v, tensor_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+              overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
+    return ATTN_ERR_INVALID_ARG;
+
+  int dev = -1;
+  const int st = prepare_device(&dev);
+  if (st != ATTN_OK) return st;
+  if (!get_encoder()) return ATTN_ERR_LAUNCH;
+
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_bhsd(&tq, q, S, BH) || !encode_bhsd(&tk, k, S, BH) || !encode_bhsd(&tv, v, S, BH) ||
+      !encode_bhsd(&to, o, S, BH))
+    return ATTN_ERR_LAUNCH;
+
+  Params prm;
+  prm.lse = lse;
+  prm.S = S;
+  prm.n_kv = static_cast<int>((S + kBlock - 1) / kBlock);
+  prm.n_qp = static_cast<int>(n_qp);
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  const dim3 grid(static_cast<unsigned>(BH * n_qp));
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED_DIM: return "unsupported head dimension (D must be 128)";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer (q/k/v/o need 16 bytes, lse 4)";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "no CUDA device, or the device is not sm_103";
+    case ATTN_ERR_LAUNCH: return "tensor-map encoding or kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int attn_device_status(unsigned int* word, int reset) {
+  if (!word) return ATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_UNSUPPORTED_DEVICE;
+  }
+  unsigned int w = 0;
+  if (cudaMemcpyFromSymbol(&w, gb300::g_attn_status, sizeof(w)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  if (reset && w != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(gb300::g_attn_status, &zero, sizeof(zero)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+  }
+  *word = w;
+  return ATTN_OK;
+}
+
+int attn_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) dense attention forward library (libattn.so).
+ *
+ * The operation (the pages: "B200 attention kernel from scratch to ~SOTA in 60 figures
+ * (CUDA/PTX)", Ch. 1 §ii "work parallelisation" and §B "online softmax"): for every batch b,
+ * head h and query row i < S, over all keys j < S (dense, non-causal, no mask),
+ *
+ *     s_ij   = scale * sum_d Q[b,h,i,d] * K[b,h,j,d]
+ *     O[b,h,i,:] = sum_j softmax_j(s_i.) * V[b,h,j,:]
+ *     lse[b,h,i] = ln sum_j exp(s_ij)          (natural log, fp32)
+ *
+ * The pages fix the scope: BF16 inputs, head_dim 128, dense, non-causal. lse is not on the
+ * pages; it is the usual FlashAttention by-product (natural log of the row's softmax
+ * denominator over the scaled scores).
+ *
+ * Thread safety: every entry point may be called from several host threads at once.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad scale, overlap, overflow */
+    ATTN_ERR_UNSUPPORTED_DIM = 2,    /* D != 128 */
+    ATTN_ERR_MISALIGNED = 3,         /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned */
+    ATTN_ERR_UNSUPPORTED_DEVICE = 4, /* no CUDA device, or the current device is not sm_103 */
+    ATTN_ERR_LAUNCH = 5,             /* tensor-map encoding or kernel launch failed */
+    ATTN_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait (see attn_device_status) */
+} attn_status;
+
+/*
+ * attn_fwd -- O = softmax(scale * Q K^T) V and lse, one fused kernel launch.
+ *
+ *   q, k, v : DEVICE pointers, BF16, contiguous [B, H, S, D] (row = one (b,h,s), 256 bytes).
+ *             Read only. 16-byte aligned.
+ *   o       : DEVICE pointer, BF16, contiguous [B, H, S, D], written. 16-byte aligned. Must not
+ *             overlap q, k, v or lse.
+ *   lse     : DEVICE pointer, fp32 [B, H, S], written (natural log); 4-byte aligned. May be
+ *             NULL, in which case lse is not written.
+ *   B, H, S : batch, heads, sequence length; each >= 1, and B*H*ceil(S/256) <= 2^31 - 1.
+ *             S need not be a multiple of 128: padded keys contribute nothing and padded
+ *             query rows are never written.
+ *   D       : head dimension; must be 128.
+ *   scale   : softmax scale applied to Q K^T (usually 1/sqrt(D)); finite and > 0. (The kernel
+ *             takes the row max on raw scores and multiplies it by the scale afterwards, as
+ *             the pages' Ch. 8 does, which is only valid for a positive scale.)
+ *   stream  : a cudaStream_t (NULL = the legacy default stream). The call is asynchronous:
+ *             it enqueues one kernel and returns; nothing is synchronised on the host.
+ *
+ * Ownership: all buffers belong to the caller. The library allocates no device memory and
+ * keeps no per-call state; it caches only per-device launch attributes.
+ *
+ * Errors: arguments are checked before any CUDA call; on any error nothing is launched and
+ * o / lse are untouched. A launch failure is reported as ATTN_ERR_LAUNCH (the CUDA error is
+ * not cleared for the caller). Faults that happen while the kernel runs surface, as usual,
+ * at the caller's next synchronisation; a kernel that gave up a bounded internal wait
+ * records it in the device status word read by attn_device_status().
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int S, int D, float scale, void* stream);
+
+/* A short, static, human-readable description of a status code. Never NULL. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_device_status -- read (and optionally clear) the current device's status word.
+ *
+ * The attention kernel bounds every internal wait (about two seconds). A CTA that gives up
+ * stops its work, releases its tensor memory, leaves its outputs incomplete and records a
+ * non-zero word here (the first failure wins). Call it after synchronising the streams that
+ * ran attn_fwd. *word receives 0 when no wait gave up. Returns ATTN_OK, or
+ * ATTN_ERR_UNSUPPORTED_DEVICE / ATTN_ERR_LAUNCH if the word could not be read.
+ */
+int attn_device_status(unsigned int* word, int reset);
+
+/* Library version, (major << 16) | minor. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

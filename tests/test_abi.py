@@ -1,0 +1,84 @@
+"""The C-ABI library: it loads, exports every symbol include/attn.h declares, and rejects bad
+arguments on the host before any CUDA call. CPU only (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_attention_forward_gb300 as attn
+from dense_attention_forward_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+# Fake, never dereferenced device addresses (16-byte aligned, disjoint).
+Q, K, V, O, L = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s*(attn_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from dense_attention_forward_gb300 import build
+        build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_status_string", "attn_version"]
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(_lib.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.attn_version() >> 16 == 1
+    for code in range(7):
+        assert lib.attn_status_string(code).decode()
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def call(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, S=256, D=128, scale=0.088):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, S, D, scale, None)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(D=64), 2), (dict(D=256), 2),
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(S=0), 1),
+    (dict(scale=0.0), 1), (dict(scale=-0.1), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(q=Q + 8), 3), (dict(o=O + 2), 3), (dict(lse=L + 2), 3),
+    (dict(o=Q), 1), (dict(o=K + 256), 1), (dict(lse=O + 1024), 1), (dict(lse=V), 1),
+    (dict(B=65536, H=65536), 1), (dict(B=1 << 20, H=1 << 10, S=4096), 1),
+])
+def test_argument_errors_are_reported_before_any_cuda_call(lib, kw, expected):
+    assert call(lib, **kw) == expected
+
+
+def test_no_device_is_reported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call(lib) == 4  # ATTN_ERR_UNSUPPORTED_DEVICE, nothing launched
+    word = ctypes.c_uint(7)
+    assert lib.attn_device_status(ctypes.byref(word), 0) == 4
+    assert lib.attn_device_status(None, 0) == 1
+
+
+def test_python_wrapper_rejects_cpu_and_wrong_dtype():
+    import torch
+    x = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.fwd(x, x, x)
+    y = torch.zeros(1, 1, 8, 128, dtype=torch.float32)
+    with pytest.raises((TypeError, ValueError)):
+        attn.fwd(y, y, y)

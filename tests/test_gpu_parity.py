@@ -1,0 +1,122 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import dense_attention_forward_gb300 as attn
+import workloads as wl
+from oracle import attn_ref as ref
+from tests.gpu_util import compare, full_parity, run_gpu, sample_rows
+from workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_workload_full():
+    w = wl.TINY
+    q, k, v = wl.make_qkv(w)
+    full_parity(q, k, v, w.scale)
+
+
+@pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 256, 257, 383, 640, 1000])
+def test_edge_lengths_full(S):
+    q, k, v = wl.make_custom(2, 3, S, seed=S)
+    full_parity(q, k, v, 1.0 / np.sqrt(128))
+
+
+@pytest.mark.parametrize("S", [300, 1024, 1500])
+def test_peaky_rows_full(S):
+    # Q and K x3 before the BF16 cast: score std ~9, rows rebase often.
+    q, k, v = wl.make_custom(1, 4, S, seed=7 + S, qk_gain=3.0)
+    full_parity(q, k, v, 1.0 / np.sqrt(128))
+
+
+def test_bf16_midpoint_output():
+    # Two equally weighted keys (q = 0) with V = 4 and 4.03125: the exact O, 4.015625, lies
+    # half-way between two BF16 numbers; the result must be one of them.
+    S, D = 2, 128
+    q = torch.zeros(1, 1, S, D, dtype=torch.bfloat16)
+    k = torch.randn(1, 1, S, D).to(torch.bfloat16)
+    v = torch.empty(1, 1, S, D, dtype=torch.bfloat16)
+    v[0, 0, 0] = 4.0
+    v[0, 0, 1] = 4.03125
+    o, lse = attn.fwd(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    vals = set(o.float().flatten().tolist())
+    assert vals <= {4.0, 4.03125}, vals
+    assert torch.allclose(lse.float().cpu(), torch.full((1, 1, S), float(np.log(2.0))), atol=1e-6)
+
+
+def test_other_scale():
+    q, k, v = wl.make_custom(1, 2, 700, seed=3)
+    full_parity(q, k, v, 0.05)
+
+
+@pytest.mark.parametrize("name", ["s4k", "s8k", "s16k", "ragged"])
+def test_full_size_workloads_sampled(name):
+    w = wl.ALL[name]
+    q, k, v = wl.make_qkv(w)
+    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale)
+    rows = sample_rows(w.S, seed=w.seed)
+    o_ref, lse_ref = ref.attention_rows(to_f64(q), to_f64(k), to_f64(v), w.scale, rows)
+    compare(o_gpu[..., rows, :], lse_gpu[..., rows], o_ref, lse_ref)
+    # Properties at every row: O is a convex combination of V rows, lse finite.
+    vf = v.float()
+    vmax = vf.amax(dim=2, keepdim=True).double().numpy()
+    vmin = vf.amin(dim=2, keepdim=True).double().numpy()
+    assert np.all(o_gpu <= vmax + 1e-2) and np.all(o_gpu >= vmin - 1e-2)
+    assert np.all(np.isfinite(lse_gpu))
+
+
+def test_guard_regions_untouched():
+    B, H, S, D = 1, 2, 200, 128
+    q, k, v = (t.cuda() for t in wl.make_custom(B, H, S, seed=11))
+    n = B * H * S * D
+    guard = 4096
+    obuf = torch.full((n + 2 * guard,), 7.0, device="cuda", dtype=torch.bfloat16)
+    lbuf = torch.full((B * H * S + 2 * 64,), 7.0, device="cuda", dtype=torch.float32)
+    o = obuf[guard:guard + n].view(B, H, S, D)
+    lse = lbuf[64:64 + B * H * S].view(B, H, S)
+    attn.fwd(q, k, v, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:guard] == 7.0) and torch.all(obuf[guard + n:] == 7.0)
+    assert torch.all(lbuf[:64] == 7.0) and torch.all(lbuf[64 + B * H * S:] == 7.0)
+    o_ref, lse_ref = ref.attention(*(to_f64(t.cpu()) for t in (q, k, v)), 1.0 / np.sqrt(128))
+    compare(to_f64(o.float().cpu()), lse.double().cpu().numpy(), o_ref, lse_ref)
+
+
+def test_side_stream_and_determinism():
+    q, k, v = (t.cuda() for t in wl.make_custom(2, 2, 777, seed=5))
+    o1, l1 = attn.fwd(q, k, v)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, l2 = attn.fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_without_lse():
+    q, k, v = (t.cuda() for t in wl.make_custom(1, 2, 333, seed=9))
+    o1, l1 = attn.fwd(q, k, v)
+    o2, l2 = attn.fwd(q, k, v, return_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o1, o2)
+
+
+def test_gpu_argument_errors():
+    x = torch.zeros(1, 1, 64, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(attn.AttnError) as e:
+        attn.fwd(x, x, x)
+    assert e.value.status == 2
+    buf = torch.zeros(1 + 1 * 1 * 64 * 128, device="cuda", dtype=torch.bfloat16)
+    y = buf[1:].view(1, 1, 64, 128)  # 2-byte offset: not 16-byte aligned
+    z = torch.zeros(1, 1, 64, 128, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(attn.AttnError) as e:
+        attn.fwd(y, z, z)
+    assert e.value.status == 3
+
+
+def test_no_wait_gave_up():
+    torch.cuda.synchronize()
+    assert attn.device_status(reset=False) == 0

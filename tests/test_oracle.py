@@ -214,3 +214,19 @@ def test_rebase_threshold_numbers_from_the_pages():
         val, dec = g[key]
         assert abs(got - val) <= 10.0 ** -dec, key
     assert max_p == 256.0
+
+
+# --- 7. the output format: no BF16 O can meet a 1.5e-2 bound everywhere once |O| >= 4 ---
+
+def test_bf16_output_cannot_always_be_within_1p5e2():
+    # Exact O = 4.015625 (two equally weighted keys with V = 4 and 4.03125, both BF16
+    # numbers); its BF16 neighbours are 4.0 and 4.03125, each 0.015625 away.
+    q = np.zeros((1, 2, 1))
+    k = np.array([[[0.3], [-1.2]]])
+    v = np.array([[[4.0], [4.03125]]])
+    o, lse = ref.attention(q, k, v, 1.0)
+    assert o[0, 0, 0] == 4.015625 and abs(lse[0, 0] - math.log(2.0)) < 1e-15
+    # 4.0 and 4.03125 are adjacent BF16 numbers (7 stored mantissa bits: spacing 2^-5 in [4, 8)).
+    assert torch.tensor([4.0, 4.03125]).to(torch.bfloat16).view(torch.int16).tolist() == [0x4080, 0x4081]
+    assert torch.tensor([4.015625]).to(torch.bfloat16).item() in (4.0, 4.03125)
+    assert min(abs(4.015625 - 4.0), abs(4.015625 - 4.03125)) == 0.015625 > 1.5e-2
