@@ -8,9 +8,9 @@ from __future__ import annotations
 
 import math
 
-from ._lib import AttnError, attn_fwd, device_status, lib  # noqa: F401
+from ._lib import AttnError, attn_fwd, attn_fwd_ex, device_status, lib  # noqa: F401
 
-__all__ = ["fwd", "attn_fwd", "device_status", "AttnError", "lib"]
+__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "device_status", "AttnError", "lib"]
 
 
 def _check(name, t, shape=None):
@@ -30,12 +30,13 @@ def _check(name, t, shape=None):
 
 
 def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True,
-        stream=None):
+        stream=None, rebase_threshold: int = 0):
     """Attention forward on the current CUDA stream (or `stream`).
 
     q, k, v: bfloat16 CUDA tensors, contiguous [B, H, S, 128]. scale defaults to 1/sqrt(128).
     Returns (o, lse) with o bfloat16 [B, H, S, 128] and lse float32 [B, H, S] (natural log),
     or (o, None) when return_lse is False. `out` / `lse` may be given preallocated.
+    rebase_threshold (0 or 8) selects the online-softmax rebase rule (see attn_fwd_ex).
     """
     import torch
     _check("q", q)
@@ -60,9 +61,9 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      lse.data_ptr() if lse is not None else None, B, H, S, D, float(scale),
-                      stream.cuda_stream)
+        st = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, S, D, float(scale),
+                         int(rebase_threshold), stream.cuda_stream)
     if st != 0:
         raise AttnError(st)
     return out, lse

@@ -20,6 +20,10 @@ SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
+    "attn_fwd_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                   ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
     "attn_version": (ctypes.c_int, []),
@@ -70,6 +74,13 @@ def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None
              S: int, D: int, scale: float, stream: int | None) -> int:
     """Direct call of the C entry point with raw addresses; returns the status code."""
     return lib().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, S, D, scale, stream)
+
+
+def attn_fwd_ex(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None, B: int, H: int,
+                S: int, D: int, scale: float, rebase_threshold_log2: int, stream: int | None) -> int:
+    """Direct call of attn_fwd_ex (rebase threshold 0 or 8); returns the status code."""
+    return lib().attn_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, S, D, scale,
+                             rebase_threshold_log2, stream)
 
 
 def device_status(reset: bool = True) -> int:

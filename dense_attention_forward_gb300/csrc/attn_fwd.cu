@@ -15,9 +15,12 @@
 //    memory, V MN-major SW128). The steady state issues PqV(i) then QqK(i+1).
 //  * Softmax (Ch. 1 §B, Ch. 8, Ch. 11): 4 warps per Q tile, one thread per row, the whole
 //    128-score row in registers; base-2 exponent with scale*log2(e) folded into one factor,
-//    row max taken on raw scores; the kept row max moves only when the tile max exceeds it
-//    by >= 8 (base 2); P is packed to BF16 pairs and stored over S in tensor memory. O is
-//    normalised by the sum of the BF16-rounded P that PV consumes; lse uses the fp32 sum.
+//    row max taken on raw scores; P is packed to BF16 pairs and stored over S in tensor
+//    memory. The kept row max follows the running max (rebase threshold 0), or, in the
+//    kRebase8 instantiation, moves only when a tile's max exceeds it by >= 8 (Ch. 11), with O
+//    then normalised by the sum of the BF16-rounded P. Only packed FP32x2 arithmetic, MUFU,
+//    conversions and byte permutes run per element: on this part scalar FP32 and IMAD work
+//    in other warps slows the tensor pipe.
 //  * Correction (Ch. 11, Ch. 12): 4 warps shared by both Q tiles rescale O in tensor memory
 //    when any row of their 32 rebased, then run the epilogue (O / l -> BF16 -> SW128 shared
 //    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
@@ -45,11 +48,10 @@ constexpr int kBlock = 128;                      // rows per Q tile and keys per
 constexpr int kHeadDim = 128;                    // D
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // one 128x128 BF16 tile: 32 KB
 constexpr int kSliceBytes = kBlock * 128;        // 128 rows x 128 B: one SW128 column of atoms
-constexpr int kStages = 3;                       // K/V ring slots
+constexpr int kStages = 4;                       // K/V ring slots
 constexpr int kThreads = 512;                    // 16 warps
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr float kRebaseLog2 = 8.0f;              // Ch. 11 threshold, base-2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
 
@@ -58,15 +60,14 @@ constexpr int kOffQ = 0;                                   // Q0, Q1 (later: O s
 constexpr int kOffKV = kOffQ + 2 * kTileBytes;             // K/V ring
 constexpr int kOffBar = kOffKV + kStages * kTileBytes;     // mbarriers
 // barrier indices
-constexpr int kBarQFull = 0;                     // [2]
-constexpr int kBarKVFull = 2;                    // [kStages]
-constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages]
+constexpr int kBarQFull = 0;                       // [2] Q_q landed (TMA bytes)
+constexpr int kBarKVFull = 2;                      // [kStages] token landed (TMA bytes)
+constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages] token consumed (MMA commit)
 constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_q in TMEM (MMA commit)
-constexpr int kBarPFull = kBarSFull + 2;           // [2] P_q in TMEM (128 softmax threads)
-constexpr int kBarOSafe = kBarPFull + 2;           // [2] O_q rescaled or untouched (128 correction threads)
-constexpr int kBarOFull = kBarOSafe + 2;           // [2] PV_q done (MMA commit)
-constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (128)
-constexpr int kBarLReady = kBarStats + 2;          // [2] final row sums published (128)
+constexpr int kBarPOReady = kBarSFull + 2;         // [2] P_q in TMEM and O_q safe: 4 softmax + 4 correction warps
+constexpr int kBarOFull = kBarPOReady + 2;         // [2] last PV_q done (MMA commit)
+constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
+constexpr int kBarLReady = kBarStats + 2;          // [2] final row sums published (4 warps)
 constexpr int kBarMmaDone = kBarLReady + 2;        // [1] drain after a failure
 constexpr int kNumBars = kBarMmaDone + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -99,7 +100,7 @@ struct Ctl {
 };
 
 __device__ __forceinline__ bool wait_slow(const Ctl& c, int b, uint32_t parity, uint32_t role,
-                                       bool watch_abort, uint64_t limit_ns) {
+                                          bool watch_abort, uint64_t limit_ns) {
   const uint32_t bar = c.bar(b);
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -129,6 +130,13 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctl& c, int b, uint32_t pari
   return __all_sync(0xffffffffu, ok);
 }
 
+// One arrival per warp, after every lane's prior shared/tensor-memory writes are ordered by
+// __syncwarp (each lane has already fenced its tcgen05 stores where that matters).
+__device__ __forceinline__ void warp_arrive(const Ctl& c, int b, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(c.bar(b));
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -140,6 +148,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// kRebase8: keep the row max until a tile's max exceeds it by 8 (base 2), the pages' Ch. 11
+// "skip O rescale"; P can then reach 2^8, and O is normalised by a second row sum over the
+// BF16-rounded P. Otherwise (threshold 0) the kept max is the running max, P <= 1 with the
+// row maximum exactly 1, and one fp32 row sum serves both O and lse.
+template <bool kRebase8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -174,11 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(c.bar(kBarSFull + q), 1);
-      mbar_init(c.bar(kBarPFull + q), 128);
-      mbar_init(c.bar(kBarOSafe + q), 128);
+      mbar_init(c.bar(kBarPOReady + q), 8);
       mbar_init(c.bar(kBarOFull + q), 1);
-      mbar_init(c.bar(kBarStats + q), 128);
-      mbar_init(c.bar(kBarLReady + q), 128);
+      mbar_init(c.bar(kBarStats + q), 4);
+      mbar_init(c.bar(kBarLReady + q), 4);
     }
     mbar_init(c.bar(kBarMmaDone), 1);
     *c.abort_flag = 0u;
@@ -195,10 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // Register split (warpgroup granularity, set at the top of each role's branch so the
-  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 80 +
-  // load/MMA WG 48 = 65536 = 512 threads x 128 registers at launch.
+  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 72 +
+  // load/MMA WG 56 = 65536 = 512 threads x 128 registers at launch.
   if (warp >= 12) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
   }
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------------ TMA producer
@@ -209,20 +221,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_o);
       const uint64_t keep = l2_policy_evict_last();   // K/V: re-read by every CTA of the head
       const uint64_t once = l2_policy_evict_first();  // Q: read once
-      bool ok = true;
-      int issued = 0;
-      for (int q = 0; q < 2 && ok; ++q) {
+      // Q0, then K0, then Q1: the first QK needs only Q0 and K0.
+      auto load_q = [&](int q) {
         const uint32_t bar = c.bar(kBarQFull + q);
         const uint32_t dst = q_smem + q * kTileBytes;
         mbar_arrive_expect_tx(bar, kTileBytes);
         tma_load_3d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, bh, once);
         tma_load_3d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, bh, once);
-      }
+      };
+      load_q(0);
+      bool ok = true;
+      int issued = 0;
+      int s = 0;
+      uint32_t empty_phase = 1;  // first pass over the ring: slots start free
       for (int t = 0; t < 2 * n; ++t) {
-        const int s = t % kStages;
-        const int use = t / kStages;
         if (t >= kStages) {
-          if (!wait_bar(c, kBarKVEmpty + s, (use - 1) & 1, kRoleLoad)) { ok = false; break; }
+          if (!wait_bar(c, kBarKVEmpty + s, empty_phase, kRoleLoad)) { ok = false; break; }
         }
         const uint32_t bar = c.bar(kBarKVFull + s);
         const uint32_t dst = kv_smem + s * kTileBytes;
@@ -232,6 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_hint(dst, map, bar, 0, row, bh, keep);
         tma_load_3d_hint(dst + kSliceBytes, map, bar, 64, row, bh, keep);
         issued = t + 1;
+        if (t == 0) load_q(1);
+        if (++s == kStages) {
+          s = 0;
+          empty_phase ^= 1u;
+        }
       }
       if (!ok) {
         // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
@@ -244,73 +263,125 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
-      // Descriptors are built once; the start-address field (bits 0-13, 16-byte units) is
-      // advanced by plain addition, which never carries out of the field here (< 256 KB).
-      // K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
+      const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
+      // Descriptors: K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
       // MN-major SW128 (V): 8-row groups along K 1024 B apart (SBO), the two 64-wide halves
-      // of N 16 KB apart (LBO).
-      const uint64_t dq0 = smem_desc_sw128(q_smem, 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(kv_smem, 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
+      // of N 16 KB apart (LBO). The start-address field (bits 0-13, 16-byte units) is moved by
+      // plain 64-bit addition; it never carries out of its field (addresses < 256 KB).
+      const uint64_t dq = smem_desc_sw128(q_smem, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(kv_smem, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
+      constexpr uint32_t kTileUnits = kTileBytes >> 4;  // one 32 KB tile in 16-byte units
+      // Bases are laundered through an opaque move so that the per-group operands are formed
+      // where they are used instead of being hoisted into registers (this warp runs with 56).
+      auto opaque64 = [](uint64_t x) {
+        asm volatile("mov.b64 %0, %0;" : "+l"(x));
+        return x;
+      };
+      auto opaque = [](uint32_t x) {
+        asm volatile("mov.b32 %0, %0;" : "+r"(x));
+        return x;
+      };
       // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
       // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further).
-      auto issue_qk = [&](int q, int slot) {
-        const uint64_t a = dq0 + static_cast<uint64_t>((q * kTileBytes) >> 4);
-        const uint64_t b = dk0 + static_cast<uint64_t>((slot * kTileBytes) >> 4);
-        const uint32_t d = tmem + static_cast<uint32_t>(q) * 128u;
-#pragma unroll 1
+      auto issue_qk = [&](uint32_t d, int q, uint32_t k_slot) {
+        const uint64_t a0 = opaque64(dq + q * kTileUnits);
+        const uint64_t b0 = opaque64(dk + k_slot * kTileUnits);
+        uint64_t a[8], b[8];
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(d, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
+          a[kk] = a0 + off;
+          b[kk] = b0 + off;
         }
+        mma8_bf16_ss<0>(d, a, b, kIdescQK);
       };
       // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
       // V rows [16kk, 16kk+16) (2048 B further per step).
-      auto issue_pv = [&](int q, int slot, bool first) {
-        const uint64_t b = dv0 + static_cast<uint64_t>((slot * kTileBytes) >> 4);
-        const uint32_t a = tmem + static_cast<uint32_t>(q) * 128u;
-        const uint32_t d = tmem + 256u + static_cast<uint32_t>(q) * 128u;
-#pragma unroll 1
+      auto issue_pv = [&](uint32_t d, uint32_t p_tmem, uint32_t v_slot, bool first) {
+        const uint32_t a0 = opaque(p_tmem);
+        const uint64_t b0 = opaque64(dv + v_slot * kTileUnits);
+        uint32_t a[8];
+        uint64_t b[8];
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_bf16_ts(d, a + kk * 8, b + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
-                      (first && kk == 0) ? 0u : 1u);
+          a[kk] = a0 + kk * 8;
+          b[kk] = b0 + kk * (2048 >> 4);
         }
+        if (first) mma8_bf16_ts<0>(d, a, b, kIdescPV);
+        else mma8_bf16_ts<1>(d, a, b, kIdescPV);
       };
-      auto full_wait = [&](int t) {
-        return wait_bar(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleMma);
-      };
+      const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
       bool ok = true;
+      // Ring position of the next token to consume: slot index and the parity of its fill.
+      int slot = 0;
+      uint32_t phase = 0;
+      auto advance = [&]() {
+        if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      };
+      // A barrier query costs a few hundred cycles of latency here, and a tcgen05.mma is
+      // only accepted when the tensor core's short queue has room. So the query for the next
+      // group's inputs is issued before the current group's MMAs and its result is examined
+      // after them: the latency overlaps work already queued. `ready` falls back to a full
+      // (bounded) wait when the probe found the phase incomplete.
+      auto ready = [&](uint32_t probed, int b, uint32_t parity) {
+        return probed != 0u || wait_bar(c, b, parity, kRoleMma);
+      };
       do {
         // prologue: Q0 K0, Q1 K0
-        if (!wait_bar(c, kBarQFull + 0, 0, kRoleMma) || !full_wait(0)) { ok = false; break; }
+        if (!wait_bar(c, kBarQFull + 0, 0, kRoleMma) || !wait_bar(c, kBarKVFull + slot, phase, kRoleMma)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        issue_qk(0, 0);
+        uint32_t k_slot = static_cast<uint32_t>(slot);
+        issue_qk(tS0, 0, k_slot);
         mma_commit(c.bar(kBarSFull + 0));
         if (!wait_bar(c, kBarQFull + 1, 0, kRoleMma)) { ok = false; break; }
         tc_fence_after();
-        issue_qk(1, 0);
+        advance();
+        // probes for tile 0's first group: V(0) and P0/O0 ready
+        uint32_t pv = mbar_test_wait(c.bar(kBarKVFull + slot), phase);
+        uint32_t pp = mbar_test_wait(c.bar(kBarPOReady + 0), 0);
+        issue_qk(tS1, 1, k_slot);
         mma_commit(c.bar(kBarSFull + 1));
-        mma_commit(c.bar(kBarKVEmpty + 0));
-        for (int i = 0; i < n && ok; ++i) {
-          const int tv = 2 * i + 1;
-          if (!full_wait(tv)) { ok = false; break; }
-          for (int q = 0; q < 2; ++q) {
-            if (!wait_bar(c, kBarPFull + q, i & 1, kRoleMma)) { ok = false; break; }
-            if (i > 0 && !wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleMma)) { ok = false; break; }
+        mma_commit(c.bar(kBarKVEmpty + k_slot));
+        for (int i = 0; i < n; ++i) {
+          const bool more = i + 1 < n;
+          const uint32_t par = static_cast<uint32_t>(i & 1);
+          // ---- Q tile 0: P0 V(i), then Q0 K(i+1)
+          if (!ready(pv, kBarKVFull + slot, phase) || !ready(pp, kBarPOReady + 0, par)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t v_slot = static_cast<uint32_t>(slot);
+          advance();
+          uint32_t pk_ = more ? mbar_test_wait(c.bar(kBarKVFull + slot), phase) : 1u;
+          issue_pv(tO0, tS0, v_slot, i == 0);
+          if (!more) mma_commit(c.bar(kBarOFull + 0));
+          if (more) {
+            if (!ready(pk_, kBarKVFull + slot, phase)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(q, tv % kStages, i == 0);
-            mma_commit(c.bar(kBarOFull + q));
-            if (q == 1) mma_commit(c.bar(kBarKVEmpty + tv % kStages));
-            if (i + 1 < n) {
-              const int tk = 2 * (i + 1);
-              if (q == 0 && !full_wait(tk)) { ok = false; break; }
-              tc_fence_after();
-              issue_qk(q, tk % kStages);
-              mma_commit(c.bar(kBarSFull + q));
-              if (q == 1) mma_commit(c.bar(kBarKVEmpty + tk % kStages));
-            }
+            k_slot = static_cast<uint32_t>(slot);
+            advance();
+            pp = mbar_test_wait(c.bar(kBarPOReady + 1), par);
+            issue_qk(tS0, 0, k_slot);
+            mma_commit(c.bar(kBarSFull + 0));
+          } else {
+            pp = mbar_test_wait(c.bar(kBarPOReady + 1), par);
+          }
+          // ---- Q tile 1: P1 V(i), then Q1 K(i+1); both tokens are then free
+          if (!ready(pp, kBarPOReady + 1, par)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(tO1, tS1, v_slot, i == 0);
+          if (!more) mma_commit(c.bar(kBarOFull + 1));
+          mma_commit(c.bar(kBarKVEmpty + v_slot));
+          if (more) {
+            // probes for the next tile's first group
+            pv = mbar_test_wait(c.bar(kBarKVFull + slot), phase);
+            pp = mbar_test_wait(c.bar(kBarPOReady + 0), par ^ 1u);
+            issue_qk(tS1, 1, k_slot);
+            mma_commit(c.bar(kBarSFull + 1));
+            mma_commit(c.bar(kBarKVEmpty + k_slot));
           }
         }
       } while (false);
@@ -330,10 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const int rem = p.S - (n - 1) * kBlock;  // valid keys in the last tile, 1..128
     float m_kept = -INFINITY;                 // kept row max, base-2 units
-    float l = 0.f;                            // running row sum of BF16 P (normalises O)
+    float l = 0.f;                            // running row sum that normalises O
     float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
     bool ok = true;
     for (int i = 0; i < n; ++i) {
+      // S_q(i) full also means every earlier MMA, so PV_q(i-1) has read P_q(i-1).
       if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[128];
@@ -345,88 +417,112 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = (j < rem) ? s[j] : -INFINITY;
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx[j] = s[j];
+      for (int j = 0; j < 4; ++j) mx[j] = fmaxf(s[2 * j], s[2 * j + 1]);
 #pragma unroll
-      for (int j = 8; j < 128; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-      const float tile_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-          sl2;
+      for (int j = 8; j < 128; j += 8) {
+        mx[0] = max3(mx[0], s[j + 0], s[j + 1]);
+        mx[1] = max3(mx[1], s[j + 2], s[j + 3]);
+        mx[2] = max3(mx[2], s[j + 4], s[j + 5]);
+        mx[3] = max3(mx[3], s[j + 6], s[j + 7]);
+      }
+      const float tile_max = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
       if (i == 0) {
         m_kept = tile_max;
       } else {
         float alpha = 1.0f;
-        if (tile_max - m_kept >= kRebaseLog2) {
+        if (kRebase8 ? (tile_max - m_kept >= 8.0f) : (tile_max > m_kept)) {
           alpha = ex2_ftz(m_kept - tile_max);
-          l *= alpha;
+          if constexpr (kRebase8) l *= alpha;
           lf *= alpha;
           m_kept = tile_max;
         }
         alpha_sm[q * kBlock + row] = alpha;
-        mbar_arrive(c.bar(kBarStats + q));
+        warp_arrive(c, kBarStats + q, lane);
       }
       const float neg_m = -m_kept;
-      float lb2[2] = {0.f, 0.f}, lf2[2] = {0.f, 0.f};
+      // lf adds the fp32 P (for the logsumexp, and for O at threshold 0). At threshold 8, lb
+      // adds the BF16-rounded P that the PV product consumes and normalises O: numerator and
+      // denominator then carry the same weights (P reaches 256 there, and a fp32-vs-BF16
+      // mismatch would show on rows dominated by one key).
+      float lb0 = 0.f, lb1 = 0.f, lb2 = 0.f, lb3 = 0.f;
+      float lf0 = 0.f, lf1 = 0.f, lf2 = 0.f, lf3 = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        const float p0 = ex2_ftz(fmaf(s[2 * j], sl2, neg_m));
-        const float p1 = ex2_ftz(fmaf(s[2 * j + 1], sl2, neg_m));
+        float x0, x1;
+        fma2(x0, x1, s[2 * j], s[2 * j + 1], sl2, sl2, neg_m, neg_m);
+        const float p0 = ex2_ftz(x0);
+        const float p1 = ex2_ftz(x1);
         pk[j] = pack_bf16x2(p0, p1);
-        // Two row sums: lb adds the BF16-rounded P that the PV product consumes and
-        // normalises O (numerator and denominator carry the same weights; with the rebase
-        // threshold P reaches 256, where a fp32-vs-BF16 mismatch shows on rows dominated by
-        // one key); lf adds the fp32 P for the logsumexp.
-        lb2[j & 1] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
-        lf2[j & 1] += p0 + p1;
+        if (j & 1) {
+          add2(lf2, lf3, lf2, lf3, p0, p1);
+        } else {
+          add2(lf0, lf1, lf0, lf1, p0, p1);
+        }
+        if constexpr (kRebase8) {
+          float b0, b1;
+          bf16x2_to_f32x2(pk[j], b0, b1);
+          if (j & 1) add2(lb2, lb3, lb2, lb3, b0, b1);
+          else add2(lb0, lb1, lb0, lb1, b0, b1);
+        }
       }
-      l += lb2[0] + lb2[1];
-      lf += lf2[0] + lf2[1];
+      lf += (lf0 + lf1) + (lf2 + lf3);
+      if constexpr (kRebase8) l += (lb0 + lb1) + (lb2 + lb3);
+      else l = lf;
       tmem_st32_x64(tS, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.bar(kBarPFull + q));
+      warp_arrive(c, kBarPOReady + q, lane);
     }
     if (ok) {
       lfin_sm[q * kBlock + row] = l;
-      mbar_arrive(c.bar(kBarLReady + q));
+      warp_arrive(c, kBarLReady + q, lane);
       const int grow = q0 + q * kBlock + row;
       if (p.lse != nullptr && grow < p.S)
         p.lse[static_cast<size_t>(bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------------ correction + epilogue
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
     bool ok = true;
-    for (int i = 1; i < n && ok; ++i) {
+    for (int i = 0; i < n && ok; ++i) {
       for (int q = 0; q < 2; ++q) {
-        if (!wait_bar_warp(c, kBarStats + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
-        const float alpha = alpha_sm[q * kBlock + row];
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-          if (!wait_bar_warp(c, kBarOFull + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
-          tc_fence_after();
+        if (i > 0) {
+          // Stats for tile i are published after S_q(i) is full, which (tcgen05.commit
+          // tracks every earlier MMA) means PV_q(i-1) has finished writing O_q.
+          if (!wait_bar_warp(c, kBarStats + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
+          const float alpha = alpha_sm[q * kBlock + row];
+          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+            tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            tmem_ld32_x32_sync(tO[q] + cc * 32, o);
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t o[32];
+              tmem_ld32_x32_sync(tO[q] + cc * 32, o);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32_x32(tO[q] + cc * 32, o);
+              for (int j = 0; j < 32; j += 2) {
+                float a0, a1;  // packed multiply: scalar FP32 math here would slow the MMAs
+                fma2(a0, a1, __uint_as_float(o[j]), __uint_as_float(o[j + 1]), alpha, alpha, 0.f, 0.f);
+                o[j] = __float_as_uint(a0);
+                o[j + 1] = __float_as_uint(a1);
+              }
+              tmem_st32_x32(tO[q] + cc * 32, o);
+            }
+            tmem_wait_st();
           }
-          tmem_wait_st();
+          tc_fence_before();
         }
-        tc_fence_before();
-        mbar_arrive(c.bar(kBarOSafe + q));
+        warp_arrive(c, kBarPOReady + q, lane);
       }
     }
     // epilogue: O / l -> BF16 -> SW128 staging in the dead Q buffer -> TMA store
     for (int q = 0; q < 2 && ok; ++q) {
       if (!wait_bar_warp(c, kBarLReady + q, 0, kRoleCorrection)) { ok = false; break; }
-      if (!wait_bar_warp(c, kBarOFull + q, (n - 1) & 1, kRoleCorrection)) { ok = false; break; }
+      if (!wait_bar_warp(c, kBarOFull + q, 0, kRoleCorrection)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.0f / lfin_sm[q * kBlock + row];
       const uint32_t stage = q_smem + q * kTileBytes;
@@ -466,9 +562,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace gb300
+
 // ==========================================================================================
 // Host side
 // ==========================================================================================
+namespace gb300 {
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -513,7 +612,9 @@ int prepare_device(int* dev_out) {
     g_dev_state[dev].store(-1, std::memory_order_release);
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
-  if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -546,9 +647,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int S, int D, float scale, void* stream) {
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int S, int D, float scale, int rebase_threshold_log2, void* stream) {
   using namespace gb300;
+  if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
   if (D != kHeadDim) return ATTN_ERR_UNSUPPORTED_DIM;
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || S <= 0) return ATTN_ERR_INVALID_ARG;
@@ -587,9 +689,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   const dim3 grid(static_cast<unsigned>(BH * n_qp));
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
+  if (rebase_threshold_log2 == 8)
+    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
+  else
+    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int S, int D, float scale, void* stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, S, D, scale, 0, stream);
 }
 
 const char* attn_status_string(int status) {

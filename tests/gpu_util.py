@@ -12,10 +12,10 @@ O_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
 
 
-def run_gpu(q, k, v, scale):
+def run_gpu(q, k, v, scale, rebase_threshold=0):
     """q, k, v: CPU BF16 [B,H,S,D]. Returns (o, lse) as float64 numpy, via the C ABI."""
     qd, kd, vd = (t.cuda() for t in (q, k, v))
-    o, lse = attn.fwd(qd, kd, vd, scale)
+    o, lse = attn.fwd(qd, kd, vd, scale, rebase_threshold=rebase_threshold)
     torch.cuda.synchronize()
     return to_f64(o.float()), lse.double().cpu().numpy()
 
@@ -48,8 +48,8 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref):
     return stats
 
 
-def full_parity(q, k, v, scale):
-    o_gpu, lse_gpu = run_gpu(q, k, v, scale)
+def full_parity(q, k, v, scale, rebase_threshold=0):
+    o_gpu, lse_gpu = run_gpu(q, k, v, scale, rebase_threshold)
     o_ref, lse_ref = ref.attention(to_f64(q), to_f64(k), to_f64(v), scale)
     return compare(o_gpu, lse_gpu, o_ref, lse_ref)
 

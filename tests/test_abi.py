@@ -30,7 +30,8 @@ def lib():
 
 
 def test_header_declares_the_boundary():
-    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_status_string", "attn_version"]
+    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_ex", "attn_status_string",
+                                  "attn_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -62,6 +63,16 @@ def call(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, S=256, D=128, scale=0.088):
 ])
 def test_argument_errors_are_reported_before_any_cuda_call(lib, kw, expected):
     assert call(lib, **kw) == expected
+
+
+@pytest.mark.parametrize("thr,expected", [(1, 1), (-8, 1), (16, 1), (7, 1)])
+def test_bad_rebase_threshold(lib, thr, expected):
+    assert lib.attn_fwd_ex(Q, K, V, O, L, 1, 1, 256, 128, 0.088, thr, None) == expected
+
+
+def test_ex_validates_like_attn_fwd(lib):
+    assert lib.attn_fwd_ex(Q, K, V, O, L, 1, 1, 256, 64, 0.088, 8, None) == 2
+    assert lib.attn_fwd_ex(Q, K, V, Q, L, 1, 1, 256, 128, 0.088, 0, None) == 1
 
 
 def test_no_device_is_reported(lib):

@@ -18,17 +18,33 @@ def test_tiny_workload_full():
     full_parity(q, k, v, w.scale)
 
 
+@pytest.mark.parametrize("thr", [0, 8])
 @pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 256, 257, 383, 640, 1000])
-def test_edge_lengths_full(S):
+def test_edge_lengths_full(S, thr):
     q, k, v = wl.make_custom(2, 3, S, seed=S)
-    full_parity(q, k, v, 1.0 / np.sqrt(128))
+    full_parity(q, k, v, 1.0 / np.sqrt(128), thr)
 
 
+@pytest.mark.parametrize("thr", [0, 8])
 @pytest.mark.parametrize("S", [300, 1024, 1500])
-def test_peaky_rows_full(S):
+def test_peaky_rows_full(S, thr):
     # Q and K x3 before the BF16 cast: score std ~9, rows rebase often.
     q, k, v = wl.make_custom(1, 4, S, seed=7 + S, qk_gain=3.0)
-    full_parity(q, k, v, 1.0 / np.sqrt(128))
+    full_parity(q, k, v, 1.0 / np.sqrt(128), thr)
+
+
+def test_rising_scores_rebase_every_tile():
+    # Key norms grow along the sequence, so every K/V tile raises the row max (by more than
+    # 8 base-2 units between the first and the last tiles): the rescale path runs at both
+    # thresholds and the two results agree with the oracle.
+    S = 1024
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(1, 2, S, 128, generator=g)
+    k = torch.randn(1, 2, S, 128, generator=g) * torch.linspace(0.2, 3.0, S).view(1, 1, S, 1)
+    v = torch.randn(1, 2, S, 128, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    for thr in (0, 8):
+        full_parity(q, k, v, 1.0 / np.sqrt(128), thr)
 
 
 def test_bf16_midpoint_output():
@@ -52,11 +68,12 @@ def test_other_scale():
     full_parity(q, k, v, 0.05)
 
 
-@pytest.mark.parametrize("name", ["s4k", "s8k", "s16k", "ragged"])
-def test_full_size_workloads_sampled(name):
+@pytest.mark.parametrize("name,thr", [("s4k", 0), ("s8k", 0), ("s16k", 0), ("ragged", 0),
+                                      ("s4k", 8), ("ragged", 8)])
+def test_full_size_workloads_sampled(name, thr):
     w = wl.ALL[name]
     q, k, v = wl.make_qkv(w)
-    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale)
+    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale, thr)
     rows = sample_rows(w.S, seed=w.seed)
     o_ref, lse_ref = ref.attention_rows(to_f64(q), to_f64(k), to_f64(v), w.scale, rows)
     compare(o_gpu[..., rows, :], lse_gpu[..., rows], o_ref, lse_ref)
