@@ -10,9 +10,11 @@
 //  * Loads (Ch. 3, Ch. 6): one TMA warp streams K and V as separate tokens through a
 //    kStages-slot ring of 32 KB SW128 slots; a slot is refilled once its last consumer (the
 //    second Q tile's QK for K, its PV for V) has committed.
-//  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 7): one elected thread issues tcgen05.mma M128 N128 K16:
-//    S_q = Q_q K^T (both K-major SW128 in shared memory) and O_q += P_q V (P from tensor
-//    memory, V MN-major SW128). The steady state issues PqV(i) then QqK(i+1).
+//  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 5, Ch. 7): tcgen05.mma M128 N128 K16, S_q = Q_q K^T (both
+//    K-major SW128 in shared memory) and O_q += P_q V (P from tensor memory, V MN-major
+//    SW128). Each softmax warpgroup's first thread issues its own Q tile's MMAs, PV_q(i) then
+//    QK_q(i+1), right after a named barrier shows P_q(i) stored; the two issuing threads take
+//    turns group by group so one Q tile's softmax overlaps the other's MMAs (ping-pong).
 //  * Softmax (Ch. 1 §B, Ch. 8, Ch. 11): 4 warps per Q tile, one thread per row, the whole
 //    128-score row in registers; base-2 exponent with scale*log2(e) folded into one factor,
 //    row max taken on raw scores; P is packed to BF16 pairs and stored over S in tensor
@@ -26,7 +28,7 @@
 //    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
-// the first 64 columns of S_q. Every mbarrier wait is bounded (about two seconds); a CTA that
+// the first 64 columns of S_q. Warp 12 loads, warp 13 owns the TMEM allocation. Every mbarrier wait is bounded (about two seconds); a CTA that
 // gives up records the failure in a device status word, drains its own TMA loads and MMAs,
 // frees its tensor memory and exits.
 #include <cuda.h>
@@ -62,14 +64,15 @@ constexpr int kOffBar = kOffKV + kStages * kTileBytes;     // mbarriers
 // barrier indices
 constexpr int kBarQFull = 0;                       // [2] Q_q landed (TMA bytes)
 constexpr int kBarKVFull = 2;                      // [kStages] token landed (TMA bytes)
-constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages] token consumed (MMA commit)
+constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages] token consumed: one MMA commit per Q tile
 constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_q in TMEM (MMA commit)
-constexpr int kBarPOReady = kBarSFull + 2;         // [2] P_q in TMEM and O_q safe: 4 softmax + 4 correction warps
-constexpr int kBarOFull = kBarPOReady + 2;         // [2] last PV_q done (MMA commit)
+constexpr int kBarOSafe = kBarSFull + 2;           // [2] O_q rescaled or left as is (4 correction warps)
+constexpr int kBarOFull = kBarOSafe + 2;           // [2] last PV_q done (MMA commit)
 constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
 constexpr int kBarLReady = kBarStats + 2;          // [2] final row sums published (4 warps)
-constexpr int kBarMmaDone = kBarLReady + 2;        // [1] drain after a failure
-constexpr int kNumBars = kBarMmaDone + 1;
+constexpr int kBarMmaDone = kBarLReady + 2;        // [2] drain after a failure (one per issuing thread)
+constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q tile q (the other leader)
+constexpr int kNumBars = kBarTurn + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffAlpha = (kOffAbort + 4 + 15) & ~15;      // float[2][128]
@@ -183,16 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(c.bar(kBarQFull + 1), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(c.bar(kBarKVFull + s), 1);
-      mbar_init(c.bar(kBarKVEmpty + s), 1);
+      mbar_init(c.bar(kBarKVEmpty + s), 2);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(c.bar(kBarSFull + q), 1);
-      mbar_init(c.bar(kBarPOReady + q), 8);
+      mbar_init(c.bar(kBarOSafe + q), 4);
       mbar_init(c.bar(kBarOFull + q), 1);
       mbar_init(c.bar(kBarStats + q), 4);
       mbar_init(c.bar(kBarLReady + q), 4);
     }
-    mbar_init(c.bar(kBarMmaDone), 1);
+    mbar_init(c.bar(kBarMmaDone + 0), 1);
+    mbar_init(c.bar(kBarMmaDone + 1), 1);
+    mbar_init(c.bar(kBarTurn + 0), 1);
+    mbar_init(c.bar(kBarTurn + 1), 1);
     *c.abort_flag = 0u;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -260,138 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-      const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
-      // Descriptors: K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
-      // MN-major SW128 (V): 8-row groups along K 1024 B apart (SBO), the two 64-wide halves
-      // of N 16 KB apart (LBO). The start-address field (bits 0-13, 16-byte units) is moved by
-      // plain 64-bit addition; it never carries out of its field (addresses < 256 KB).
-      const uint64_t dq = smem_desc_sw128(q_smem, 16, 1024);
-      const uint64_t dk = smem_desc_sw128(kv_smem, 16, 1024);
-      const uint64_t dv = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
-      constexpr uint32_t kTileUnits = kTileBytes >> 4;  // one 32 KB tile in 16-byte units
-      // Bases are laundered through an opaque move so that the per-group operands are formed
-      // where they are used instead of being hoisted into registers (this warp runs with 56).
-      auto opaque64 = [](uint64_t x) {
-        asm volatile("mov.b64 %0, %0;" : "+l"(x));
-        return x;
-      };
-      auto opaque = [](uint32_t x) {
-        asm volatile("mov.b32 %0, %0;" : "+r"(x));
-        return x;
-      };
-      // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
-      // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further).
-      auto issue_qk = [&](uint32_t d, int q, uint32_t k_slot) {
-        const uint64_t a0 = opaque64(dq + q * kTileUnits);
-        const uint64_t b0 = opaque64(dk + k_slot * kTileUnits);
-        uint64_t a[8], b[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
-          a[kk] = a0 + off;
-          b[kk] = b0 + off;
-        }
-        mma8_bf16_ss<0>(d, a, b, kIdescQK);
-      };
-      // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
-      // V rows [16kk, 16kk+16) (2048 B further per step).
-      auto issue_pv = [&](uint32_t d, uint32_t p_tmem, uint32_t v_slot, bool first) {
-        const uint32_t a0 = opaque(p_tmem);
-        const uint64_t b0 = opaque64(dv + v_slot * kTileUnits);
-        uint32_t a[8];
-        uint64_t b[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          a[kk] = a0 + kk * 8;
-          b[kk] = b0 + kk * (2048 >> 4);
-        }
-        if (first) mma8_bf16_ts<0>(d, a, b, kIdescPV);
-        else mma8_bf16_ts<1>(d, a, b, kIdescPV);
-      };
-      const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
-      bool ok = true;
-      // Ring position of the next token to consume: slot index and the parity of its fill.
-      int slot = 0;
-      uint32_t phase = 0;
-      auto advance = [&]() {
-        if (++slot == kStages) { slot = 0; phase ^= 1u; }
-      };
-      // A barrier query costs a few hundred cycles of latency here, and a tcgen05.mma is
-      // only accepted when the tensor core's short queue has room. So the query for the next
-      // group's inputs is issued before the current group's MMAs and its result is examined
-      // after them: the latency overlaps work already queued. `ready` falls back to a full
-      // (bounded) wait when the probe found the phase incomplete.
-      auto ready = [&](uint32_t probed, int b, uint32_t parity) {
-        return probed != 0u || wait_bar(c, b, parity, kRoleMma);
-      };
-      do {
-        // prologue: Q0 K0, Q1 K0
-        if (!wait_bar(c, kBarQFull + 0, 0, kRoleMma) || !wait_bar(c, kBarKVFull + slot, phase, kRoleMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t k_slot = static_cast<uint32_t>(slot);
-        issue_qk(tS0, 0, k_slot);
-        mma_commit(c.bar(kBarSFull + 0));
-        if (!wait_bar(c, kBarQFull + 1, 0, kRoleMma)) { ok = false; break; }
-        tc_fence_after();
-        advance();
-        // probes for tile 0's first group: V(0) and P0/O0 ready
-        uint32_t pv = mbar_test_wait(c.bar(kBarKVFull + slot), phase);
-        uint32_t pp = mbar_test_wait(c.bar(kBarPOReady + 0), 0);
-        issue_qk(tS1, 1, k_slot);
-        mma_commit(c.bar(kBarSFull + 1));
-        mma_commit(c.bar(kBarKVEmpty + k_slot));
-        for (int i = 0; i < n; ++i) {
-          const bool more = i + 1 < n;
-          const uint32_t par = static_cast<uint32_t>(i & 1);
-          // ---- Q tile 0: P0 V(i), then Q0 K(i+1)
-          if (!ready(pv, kBarKVFull + slot, phase) || !ready(pp, kBarPOReady + 0, par)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t v_slot = static_cast<uint32_t>(slot);
-          advance();
-          uint32_t pk_ = more ? mbar_test_wait(c.bar(kBarKVFull + slot), phase) : 1u;
-          issue_pv(tO0, tS0, v_slot, i == 0);
-          if (!more) mma_commit(c.bar(kBarOFull + 0));
-          if (more) {
-            if (!ready(pk_, kBarKVFull + slot, phase)) { ok = false; break; }
-            tc_fence_after();
-            k_slot = static_cast<uint32_t>(slot);
-            advance();
-            pp = mbar_test_wait(c.bar(kBarPOReady + 1), par);
-            issue_qk(tS0, 0, k_slot);
-            mma_commit(c.bar(kBarSFull + 0));
-          } else {
-            pp = mbar_test_wait(c.bar(kBarPOReady + 1), par);
-          }
-          // ---- Q tile 1: P1 V(i), then Q1 K(i+1); both tokens are then free
-          if (!ready(pp, kBarPOReady + 1, par)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(tO1, tS1, v_slot, i == 0);
-          if (!more) mma_commit(c.bar(kBarOFull + 1));
-          mma_commit(c.bar(kBarKVEmpty + v_slot));
-          if (more) {
-            // probes for the next tile's first group
-            pv = mbar_test_wait(c.bar(kBarKVFull + slot), phase);
-            pp = mbar_test_wait(c.bar(kBarPOReady + 0), par ^ 1u);
-            issue_qk(tS1, 1, k_slot);
-            mma_commit(c.bar(kBarSFull + 1));
-            mma_commit(c.bar(kBarKVEmpty + k_slot));
-          }
-        }
-      } while (false);
-      if (!ok) {
-        // Give up: make sure every MMA issued so far has finished before TMEM is freed.
-        mma_commit(c.bar(kBarMmaDone));
-        wait_slow(c, kBarMmaDone, 0, kRoleMma, false, kDrainLimitNs);
-      }
-    }
-    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax (Q tile q)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
@@ -404,8 +278,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;                            // running row sum that normalises O
     float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      // S_q(i) full also means every earlier MMA, so PV_q(i-1) has read P_q(i-1).
+
+    // The warpgroup's first thread issues this Q tile's MMAs: PV_q(i) as soon as the four
+    // warps have stored P_q(i) (a named barrier, no mbarrier round trip through another
+    // warp), then QK_q(i+1). The two leaders take turns, group by group (G_q(0) = QK_q(0),
+    // G_q(j) = PV_q(j-1) + QK_q(j)), in the order G0(0) G1(0) G0(1) G1(1) ...: one Q tile's
+    // softmax then runs while the tensor pipe works for the other (the pages' two-Q-tile
+    // ping-pong); without the turns both tiles drift into lockstep and the pipe idles while
+    // both softmaxes run. Turn barrier kBarTurn + q completes once per group the other
+    // leader has issued.
+    const bool leader = (warp & 3) == 0 && lane == 0;
+    const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+    const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
+    constexpr uint32_t kTileUnits = kTileBytes >> 4;            // one 32 KB tile, 16-byte units
+    const uint32_t tSq = tmem + q * 128u, tOq = tmem + 256u + q * 128u;
+    // Descriptors: K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
+    // MN-major SW128 (V): 8-row groups along K 1024 B apart (SBO), the two 64-wide halves
+    // of N 16 KB apart (LBO). The start-address field (bits 0-13, 16-byte units) is moved by
+    // plain 64-bit addition; it never carries out of its field (addresses < 256 KB).
+    const uint64_t dq = smem_desc_sw128(q_smem + q * kTileBytes, 16, 1024);
+    const uint64_t dk = smem_desc_sw128(kv_smem, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
+    // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
+    // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further).
+    auto issue_qk = [&](uint32_t k_slot) {
+      uint64_t a[8], b[8];
+      const uint64_t b0 = dk + k_slot * kTileUnits;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
+        a[kk] = dq + off;
+        b[kk] = b0 + off;
+      }
+      mma8_bf16_ss<0>(tSq, a, b, kIdescQK);
+    };
+    // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
+    // V rows [16kk, 16kk+16) (2048 B further per step).
+    auto issue_pv = [&](uint32_t v_slot, bool first) {
+      uint32_t a[8];
+      uint64_t b[8];
+      const uint64_t b0 = dv + v_slot * kTileUnits;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        a[kk] = tSq + kk * 8;
+        b[kk] = b0 + kk * (2048 >> 4);
+      }
+      if (first) mma8_bf16_ts<0>(tOq, a, b, kIdescPV);
+      else mma8_bf16_ts<1>(tOq, a, b, kIdescPV);
+    };
+    // K(i) is token 2i and V(i) token 2i+1 of the ring; token t sits in slot t % kStages
+    // and its fill completes phase t / kStages of that slot's barrier.
+    auto token_bar = [&](int t) { return kBarKVFull + t % kStages; };
+    auto token_par = [&](int t) { return static_cast<uint32_t>((t / kStages) & 1); };
+    if (leader) {
+      ok = wait_bar(c, kBarQFull + q, 0, kRoleSoftmax) && wait_bar(c, token_bar(0), 0, kRoleSoftmax) &&
+           (q == 0 || wait_bar(c, kBarTurn + 1, 0, kRoleSoftmax));
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+        mma_commit(c.bar(kBarSFull + q));
+        mma_commit(c.bar(kBarKVEmpty + 0));
+        tc_fence_before();
+        mbar_arrive(c.bar(kBarTurn + (q ^ 1)));  // G_q(0) issued
+      }
+    }
+    __syncwarp();
+
+    for (int i = 0; i < n && ok; ++i) {
+      // S_q(i) full also means every earlier MMA of this Q tile, so PV_q(i-1) has read
+      // P_q(i-1).
       if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[128];
@@ -474,8 +415,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32_x64(tS, pk);
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(c, kBarPOReady + q, lane);
+      named_bar_sync(2 + q, 128);  // P_q(i) stored by all four warps
+      if (leader) {
+        tc_fence_after();
+        const int tv = 2 * i + 1, tk = 2 * i + 2;
+        const bool more = i + 1 < n;
+        // V(i), O_q safe for tile i (the correction warps' rescale, i >= 1), K(i+1) and this
+        // leader's turn for group G_q(i+1): the four probes are issued together so their
+        // latencies overlap. Leader 0's turn for G0(i+1) follows G1(i) (phase i of its turn
+        // barrier); leader 1's for G1(i+1) follows G0(i+1) (phase i+1).
+        const uint32_t turn_par = static_cast<uint32_t>((q == 0 ? i : i + 1) & 1);
+        const uint32_t rdy = mbar_probe4(c.bar(token_bar(tv)), token_par(tv),
+                                         c.bar(kBarOSafe + q), static_cast<uint32_t>((i - 1) & 1),
+                                         c.bar(token_bar(more ? tk : tv)), token_par(more ? tk : tv),
+                                         c.bar(kBarTurn + q), turn_par);
+        ok = ((rdy & 1u) || wait_bar(c, token_bar(tv), token_par(tv), kRoleSoftmax)) &&
+             (i == 0 || (rdy & 2u) || wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleSoftmax)) &&
+             (!more || (rdy & 4u) || wait_bar(c, token_bar(tk), token_par(tk), kRoleSoftmax)) &&
+             ((rdy & 8u) || wait_bar(c, kBarTurn + q, turn_par, kRoleSoftmax));
+        if (ok) {
+          tc_fence_after();
+          issue_pv(static_cast<uint32_t>(tv % kStages), i == 0);
+          mma_commit(c.bar(kBarKVEmpty + tv % kStages));
+          if (more) {
+            issue_qk(static_cast<uint32_t>(tk % kStages));
+            mma_commit(c.bar(kBarSFull + q));
+            mma_commit(c.bar(kBarKVEmpty + tk % kStages));
+          } else {
+            mma_commit(c.bar(kBarOFull + q));
+          }
+          // Hand the turn over (leader 1's last group has no successor).
+          if (q == 0 || more) {
+            tc_fence_before();
+            mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
+    if (leader && !ok) {
+      // Give up: make sure every MMA this thread issued has finished before TMEM is freed.
+      mma_commit(c.bar(kBarMmaDone + q));
+      wait_slow(c, kBarMmaDone + q, 0, kRoleSoftmax, false, kDrainLimitNs);
+    }
+    __syncwarp();
     if (ok) {
       lfin_sm[q * kBlock + row] = l;
       warp_arrive(c, kBarLReady + q, lane);
@@ -490,11 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
+    for (int i = 1; i < n && ok; ++i) {
       for (int q = 0; q < 2; ++q) {
-        if (i > 0) {
+        {
           // Stats for tile i are published after S_q(i) is full, which (tcgen05.commit
-          // tracks every earlier MMA) means PV_q(i-1) has finished writing O_q.
+          // tracks every earlier MMA of that Q tile) means PV_q(i-1) has finished writing O_q.
           if (!wait_bar_warp(c, kBarStats + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
           const float alpha = alpha_sm[q * kBlock + row];
           if (__any_sync(0xffffffffu, alpha != 1.0f)) {
@@ -516,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
         }
-        warp_arrive(c, kBarPOReady + q, lane);
+        warp_arrive(c, kBarOSafe + q, lane);
       }
     }
     // epilogue: O / l -> BF16 -> SW128 staging in the dead Q buffer -> TMA store

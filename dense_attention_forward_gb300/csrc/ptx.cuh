@@ -81,6 +81,51 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity
   return ok;
 }
 
+// Three non-blocking probes in one block: their latencies overlap. Bit i of the result is
+// set if phase par_i of barrier bar_i had completed.
+__device__ __forceinline__ uint32_t mbar_probe3(uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                                uint32_t par1, uint32_t bar2, uint32_t par2) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t.reg .b32 t0, t1, t2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "selp.u32 t0, 1, 0, q0;\n\t"
+      "selp.u32 t1, 2, 0, q1;\n\t"
+      "selp.u32 t2, 4, 0, q2;\n\t"
+      "or.b32 t0, t0, t1;\n\t"
+      "or.b32 %0, t0, t2;\n}\n"
+      : "=r"(r)
+      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1), "r"(bar2), "r"(par2)
+      : "memory");
+  return r;
+}
+
+// Four probes in one block (bits 0-3).
+__device__ __forceinline__ uint32_t mbar_probe4(uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                                uint32_t par1, uint32_t bar2, uint32_t par2,
+                                                uint32_t bar3, uint32_t par3) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2, q3;\n\t.reg .b32 t0, t1, t2, t3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+      "selp.u32 t0, 1, 0, q0;\n\t"
+      "selp.u32 t1, 2, 0, q1;\n\t"
+      "selp.u32 t2, 4, 0, q2;\n\t"
+      "selp.u32 t3, 8, 0, q3;\n\t"
+      "or.b32 t0, t0, t1;\n\t"
+      "or.b32 t2, t2, t3;\n\t"
+      "or.b32 %0, t0, t2;\n}\n"
+      : "=r"(r)
+      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1), "r"(bar2), "r"(par2), "r"(bar3), "r"(par3)
+      : "memory");
+  return r;
+}
+
 // ---------------------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------------------
@@ -278,6 +323,62 @@ __device__ __forceinline__ void mma8_bf16_ts(uint32_t d_tmem, const uint32_t (&a
       "r"(idesc), "n"(kAcc0)
       : "memory");
 }
+
+// The same eight-MMA groups, with up to two mbarrier probes issued in the same asm block
+// ahead of the MMAs and their predicates read after them: a probe's result takes a few
+// hundred cycles to come back inside the running kernel, and this way that latency overlaps
+// the MMAs instead of stalling the issuing thread before them. probe[i] receives 1 if phase
+// `parity[i]` of barrier `bar[i]` had completed (bar == 0 with nprobes < 2 skips the second).
+#define GB300_MMA8_BODY(A0, A1, A2, A3, A4, A5, A6, A7)                                      \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A0 ", %12, %20, p0;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A1 ", %13, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A2 ", %14, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A3 ", %15, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A4 ", %16, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A5 ", %17, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A6 ", %18, %20, p1;\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A7 ", %19, %20, p1;\n\t"
+
+template <int kAcc0>
+__device__ __forceinline__ void mma8_bf16_ss_probe(uint32_t d_tmem, const uint64_t (&a)[8],
+                                                   const uint64_t (&b)[8], uint32_t idesc,
+                                                   uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                                   uint32_t par1, uint32_t& probe0, uint32_t& probe1) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, q0, q1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%22], %23;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%24], %25;\n\t"
+      "setp.ne.b32 p0, %21, 0;\n\t"
+      "setp.eq.u32 p1, %20, %20;\n\t" GB300_MMA8_BODY("%3", "%4", "%5", "%6", "%7", "%8", "%9", "%10")
+      "selp.u32 %0, 1, 0, q0;\n\t"
+      "selp.u32 %1, 1, 0, q1;\n}\n"
+      : "=r"(probe0), "=r"(probe1)
+      : "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]),
+        "l"(a[7]), "n"(0), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+        "l"(b[6]), "l"(b[7]), "r"(idesc), "n"(kAcc0), "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
+      : "memory");
+}
+
+template <int kAcc0>
+__device__ __forceinline__ void mma8_bf16_ts_probe(uint32_t d_tmem, const uint32_t (&a)[8],
+                                                   const uint64_t (&b)[8], uint32_t idesc,
+                                                   uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                                   uint32_t par1, uint32_t& probe0, uint32_t& probe1) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, q0, q1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%22], %23;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%24], %25;\n\t"
+      "setp.ne.b32 p0, %21, 0;\n\t"
+      "setp.eq.u32 p1, %20, %20;\n\t" GB300_MMA8_BODY("[%3]", "[%4]", "[%5]", "[%6]", "[%7]", "[%8]", "[%9]", "[%10]")
+      "selp.u32 %0, 1, 0, q0;\n\t"
+      "selp.u32 %1, 1, 0, q1;\n}\n"
+      : "=r"(probe0), "=r"(probe1)
+      : "r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
+        "r"(a[7]), "n"(0), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
+        "l"(b[6]), "l"(b[7]), "r"(idesc), "n"(kAcc0), "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
+      : "memory");
+}
+#undef GB300_MMA8_BODY
 
 // The two BF16 halves of `pk` as FP32 values, with byte permutes (integer ALU pipe).
 // On this part FMA-pipe instructions issued by other warps (scalar FFMA/FADD/FMUL, IMAD,
