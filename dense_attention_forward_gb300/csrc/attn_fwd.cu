@@ -28,7 +28,8 @@
 //    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
-// the first 64 columns of S_q. Warp 12 loads, warp 13 owns the TMEM allocation. Every mbarrier wait is bounded (about two seconds); a CTA that
+// the first 64 columns of S_q. Warp 12 loads, warp 13 owns the TMEM allocation. Every
+// mbarrier wait is bounded (about two seconds); a CTA that
 // gives up records the failure in a device status word, drains its own TMA loads and MMAs,
 // frees its tensor memory and exits.
 #include <cuda.h>
