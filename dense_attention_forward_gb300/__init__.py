@@ -8,9 +8,9 @@ from __future__ import annotations
 
 import math
 
-from ._lib import AttnError, attn_fwd, attn_fwd_ex, device_status, lib  # noqa: F401
+from ._lib import AttnError, attn_fwd, attn_fwd_ex, attn_fwd_strided, device_status, lib  # noqa: F401
 
-__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "device_status", "AttnError", "lib"]
+__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "AttnError", "lib"]
 
 
 def _check(name, t, shape=None):
@@ -21,10 +21,10 @@ def _check(name, t, shape=None):
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous [B, H, S, D]")
     if t.dim() != 4:
         raise ValueError(f"{name} must be 4-D [B, H, S, D]")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must have a contiguous head dimension")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
@@ -33,9 +33,11 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
         stream=None, rebase_threshold: int = 0):
     """Attention forward on the current CUDA stream (or `stream`).
 
-    q, k, v: bfloat16 CUDA tensors, contiguous [B, H, S, 128]. scale defaults to 1/sqrt(128).
-    Returns (o, lse) with o bfloat16 [B, H, S, 128] and lse float32 [B, H, S] (natural log),
-    or (o, None) when return_lse is False. `out` / `lse` may be given preallocated.
+    q, k, v: bfloat16 CUDA tensors shaped [B, H, S, 128] with a contiguous last dimension;
+    any other strides (e.g. a [B, S, H, D] buffer viewed through transpose(1, 2)) are passed
+    to the kernel as they are. scale defaults to 1/sqrt(128).
+    Returns (o, lse) with o bfloat16 [B, H, S, 128] (contiguous unless `out` is given) and
+    lse float32 [B, H, S] (natural log), or (o, None) when return_lse is False.
     rebase_threshold (0 or 8) selects the online-softmax rebase rule (see attn_fwd_ex).
     """
     import torch
@@ -48,7 +50,7 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, H, S, D), device=q.device, dtype=torch.bfloat16)
     else:
         _check("out", out, q.shape)
     if return_lse:
@@ -60,10 +62,16 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
         lse = None
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    lse_ptr = lse.data_ptr() if lse is not None else None
     with torch.cuda.device(q.device):
-        st = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         lse.data_ptr() if lse is not None else None, B, H, S, D, float(scale),
-                         int(rebase_threshold), stream.cuda_stream)
+        if all(t.is_contiguous() for t in (q, k, v, out)):
+            st = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                             B, H, S, D, float(scale), int(rebase_threshold), stream.cuda_stream)
+        else:
+            st = attn_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                                  B, H, S, D, float(scale), q.stride()[:3], k.stride()[:3],
+                                  v.stride()[:3], out.stride()[:3], int(rebase_threshold),
+                                  stream.cuda_stream)
     if st != 0:
         raise AttnError(st)
     return out, lse

@@ -92,6 +92,7 @@ __device__ unsigned int g_attn_status = 0;
 struct Params {
   float* lse;
   int S;            // sequence length
+  int H;            // heads (the tensor maps are 4-D: {D, S, H, B})
   int n_kv;         // ceil(S / 128)
   int n_qp;         // ceil(S / 256): CTAs per (b, h)
   float scale_log2; // scale * log2(e)
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int qp = blockIdx.x % p.n_qp;
   const int bh = blockIdx.x / p.n_qp;
+  const int hh = bh % p.H, bb = bh / p.H;
   const int q0 = qp * 2 * kBlock;
   const int n = p.n_kv;
 
@@ -233,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar = c.bar(kBarQFull + q);
         const uint32_t dst = q_smem + q * kTileBytes;
         mbar_arrive_expect_tx(bar, kTileBytes);
-        tma_load_3d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, bh, once);
-        tma_load_3d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, bh, once);
+        tma_load_4d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, hh, bb, once);
+        tma_load_4d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, hh, bb, once);
       };
       load_q(0);
       bool ok = true;
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         const int row = (t >> 1) * kBlock;
         mbar_arrive_expect_tx(bar, kTileBytes);
-        tma_load_3d_hint(dst, map, bar, 0, row, bh, keep);
-        tma_load_3d_hint(dst + kSliceBytes, map, bar, 64, row, bh, keep);
+        tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, keep);
+        tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
         issued = t + 1;
         if (t == 0) load_q(1);
         if (++s == kStages) {
@@ -529,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (warp == 8 && lane == 0 && q0 + q * kBlock < p.S) {
-        tma_store_3d(&tm_o, stage, 0, q0 + q * kBlock, bh);
-        tma_store_3d(&tm_o, stage + kSliceBytes, 64, q0 + q * kBlock, bh);
+        tma_store_4d(&tm_o, stage, 0, q0 + q * kBlock, hh, bb);
+        tma_store_4d(&tm_o, stage + kSliceBytes, 64, q0 + q * kBlock, hh, bb);
         tma_store_commit();
       }
     }
@@ -607,18 +609,46 @@ int prepare_device(int* dev_out) {
   return ATTN_OK;
 }
 
-// [D, S, B*H] BF16 view of a contiguous [B, H, S, D] tensor; 64x128 boxes, 128-byte swizzle.
-bool encode_bhsd(CUtensorMap* map, const void* ptr, int S, long long BH) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(S),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
-                                 static_cast<cuuint64_t>(S) * kHeadDim * 2};
-  const cuuint32_t box[3] = {64, kBlock, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+// A BF16 [B, H, S, D] tensor with element strides (sb, sh, ss) and unit stride along D, as a
+// 4-D tensor map {D, S, H, B}; 64x128 boxes, 128-byte swizzle, zero fill past S.
+bool encode_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, const long long (&st)[3]) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                                 static_cast<cuuint64_t>(st[0]) * 2};
+  const cuuint32_t box[4] = {64, kBlock, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Bytes from the first to one past the last element a strided [B, H, S, 128] tensor touches.
+size_t span_bytes(int B, int H, int S, const long long (&st)[3]) {
+  return static_cast<size_t>((static_cast<long long>(B - 1) * st[0] + static_cast<long long>(H - 1) * st[1] +
+                              static_cast<long long>(S - 1) * st[2] + kHeadDim) *
+                             2);
+}
+
+// Element strides that map distinct (b, h, s, d) to distinct addresses: sorted by size,
+// each stride covers the extent of the next smaller one (a row of 128 for the smallest).
+bool injective(int B, int H, int S, const long long (&st)[3]) {
+  long long v[3][2] = {{st[0], B}, {st[1], H}, {st[2], S}};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (v[j][0] < v[i][0]) {
+        std::swap(v[i][0], v[j][0]);
+        std::swap(v[i][1], v[j][1]);
+      }
+  long long need = kHeadDim;
+  for (int i = 0; i < 3; ++i) {
+    if (v[i][1] > 1) {
+      if (v[i][0] < need) return false;
+      need = v[i][0] * v[i][1];
+    }
+  }
+  return true;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -631,43 +661,56 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int S, int D, float scale, int rebase_threshold_log2, void* stream) {
+static int attn_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int S, int D, float scale, const long long* qs, const long long* ks,
+                       const long long* vs, const long long* os, int rebase_threshold_log2,
+                       void* stream) {
   using namespace gb300;
   if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
   if (D != kHeadDim) return ATTN_ERR_UNSUPPORTED_DIM;
-  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !qs || !ks || !vs || !os) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || S <= 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qp = (static_cast<long long>(S) + 2 * kBlock - 1) / (2 * kBlock);
   if (BH > (1ll << 31) - 1 || BH * n_qp > (1ll << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  long long st[4][3];
+  const long long* in[4] = {qs, ks, vs, os};
+  for (int t = 0; t < 4; ++t) {
+    for (int j = 0; j < 3; ++j) {
+      st[t][j] = in[t][j];
+      // TMA: strides in bytes are positive multiples of 16 below 2^40.
+      if (st[t][j] <= 0 || st[t][j] >= (1ll << 39)) return ATTN_ERR_INVALID_ARG;
+      if (st[t][j] % 8 != 0) return ATTN_ERR_MISALIGNED;
+    }
+  }
+  if (!injective(B, H, S, st[3])) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
     return ATTN_ERR_MISALIGNED;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
-  const size_t tensor_bytes = static_cast<size_t>(BH) * S * kHeadDim * 2;
+  const size_t qb = span_bytes(B, H, S, st[0]), kb = span_bytes(B, H, S, st[1]);
+  const size_t vb = span_bytes(B, H, S, st[2]), ob = span_bytes(B, H, S, st[3]);
   const size_t lse_bytes = static_cast<size_t>(BH) * S * 4;
-  if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
-      overlaps(o, tensor_bytes, v, tensor_bytes))
-    return ATTN_ERR_INVALID_ARG;
-  if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
-              overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
+  if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, vb)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (overlaps(lse, lse_bytes, q, qb) || overlaps(lse, lse_bytes, k, kb) ||
+              overlaps(lse, lse_bytes, v, vb) || overlaps(lse, lse_bytes, o, ob)))
     return ATTN_ERR_INVALID_ARG;
 
   int dev = -1;
-  const int st = prepare_device(&dev);
-  if (st != ATTN_OK) return st;
+  const int status = prepare_device(&dev);
+  if (status != ATTN_OK) return status;
   if (!get_encoder()) return ATTN_ERR_LAUNCH;
 
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bhsd(&tq, q, S, BH) || !encode_bhsd(&tk, k, S, BH) || !encode_bhsd(&tv, v, S, BH) ||
-      !encode_bhsd(&to, o, S, BH))
+  if (!encode_4d(&tq, q, B, H, S, st[0]) || !encode_4d(&tk, k, B, H, S, st[1]) ||
+      !encode_4d(&tv, v, B, H, S, st[2]) || !encode_4d(&to, o, B, H, S, st[3]))
     return ATTN_ERR_LAUNCH;
 
   Params prm;
   prm.lse = lse;
   prm.S = S;
+  prm.H = H;
   prm.n_kv = static_cast<int>((S + kBlock - 1) / kBlock);
   prm.n_qp = static_cast<int>(n_qp);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -679,6 +722,21 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
     attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int S, int D, float scale, int rebase_threshold_log2, void* stream) {
+  // Contiguous [B, H, S, D]: element strides (H*S*D, S*D, D).
+  const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, stream);
+}
+
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int S, int D, float scale, const long long* q_strides, const long long* k_strides,
+                     const long long* v_strides, const long long* o_strides, int rebase_threshold_log2,
+                     void* stream) {
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, q_strides, k_strides, v_strides, o_strides,
+                     rebase_threshold_log2, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -81,6 +81,27 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 int B, int H, int S, int D, float scale, int rebase_threshold_log2,
                 void* stream);
 
+/*
+ * attn_fwd_strided -- attn_fwd_ex on strided tensors (no copies): [B, S, H, D], slices of a
+ * packed QKV buffer, and so on. The head dimension must be contiguous (unit stride).
+ *
+ *   q_strides, k_strides, v_strides, o_strides : HOST pointers to 3 element strides each,
+ *             {batch, head, sequence}; element (b, h, s, d) of q is q + b*qs[0] + h*qs[1] +
+ *             s*qs[2] + d. Every stride must be > 0 and a multiple of 8 elements (16 bytes,
+ *             a TMA requirement); the output strides must not map two elements to one
+ *             address. Read during the call only.
+ *   lse     : still a contiguous fp32 [B, H, S] (or NULL).
+ *   Overlap between o / lse and the inputs is checked on the address ranges the strides span.
+ *   Contiguous [B, H, S, D] corresponds to strides {H*S*D, S*D, D}; [B, S, H, D] to
+ *   {S*H*D, D, H*D}.
+ * Other arguments, errors and ownership as attn_fwd_ex.
+ */
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int S, int D, float scale,
+                     const long long* q_strides, const long long* k_strides,
+                     const long long* v_strides, const long long* o_strides,
+                     int rebase_threshold_log2, void* stream);
+
 /* A short, static, human-readable description of a status code. Never NULL. */
 const char* attn_status_string(int status);
 

@@ -30,8 +30,8 @@ def lib():
 
 
 def test_header_declares_the_boundary():
-    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_ex", "attn_status_string",
-                                  "attn_version"]
+    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided",
+                                  "attn_status_string", "attn_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -73,6 +73,35 @@ def test_bad_rebase_threshold(lib, thr, expected):
 def test_ex_validates_like_attn_fwd(lib):
     assert lib.attn_fwd_ex(Q, K, V, O, L, 1, 1, 256, 64, 0.088, 8, None) == 2
     assert lib.attn_fwd_ex(Q, K, V, Q, L, 1, 1, 256, 128, 0.088, 0, None) == 1
+
+
+def strided(lib, qs, ks=None, vs=None, os_=None, B=2, H=3, S=256, q=Q, o=O, lse=L):
+    arr = ctypes.c_longlong * 3
+    ks, vs, os_ = ks or qs, vs or qs, os_ or qs
+    return lib.attn_fwd_strided(q, K, V, o, lse, B, H, S, 128, 0.088, arr(*qs), arr(*ks), arr(*vs),
+                                arr(*os_), 0, None)
+
+
+BHSD = (3 * 256 * 128, 256 * 128, 128)
+BSHD = (256 * 3 * 128, 128, 3 * 128)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(qs=(0, 256 * 128, 128)), 1),                       # zero stride
+    (dict(qs=(-1, 256 * 128, 128)), 1),                      # negative
+    (dict(qs=(3 * 256 * 128, 256 * 128, 132)), 3),           # not a multiple of 16 bytes
+    (dict(qs=BHSD, os_=(128, 128, 128)), 1),                 # output rows would collide
+    (dict(qs=BHSD, os_=(256 * 128, 256 * 128, 128)), 1),     # batch and head overlap in o
+    (dict(qs=BSHD, o=Q + 128 * 2), 1),                       # o inside q's span
+])
+def test_strided_argument_errors(lib, kw, expected):
+    assert strided(lib, **kw) == expected
+
+
+def test_strided_null_strides(lib):
+    arr = ctypes.c_longlong * 3
+    assert lib.attn_fwd_strided(Q, K, V, O, L, 1, 1, 256, 128, 0.088, None, arr(*BHSD), arr(*BHSD),
+                                arr(*BHSD), 0, None) == 1
 
 
 def test_no_device_is_reported(lib):

@@ -85,6 +85,35 @@ def test_full_size_workloads_sampled(name, thr):
     assert np.all(np.isfinite(lse_gpu))
 
 
+@pytest.mark.parametrize("thr", [0, 8])
+def test_bshd_layout(thr):
+    # [B, S, H, D] buffers viewed as [B, H, S, D] through transpose(1, 2): the kernel reads
+    # and writes them in place through 4-D tensor maps.
+    B, H, S, D = 2, 3, 515, 128
+    q, k, v = wl.make_custom(B, H, S, seed=31)
+    qd, kd, vd = (t.transpose(1, 2).contiguous().cuda().transpose(1, 2) for t in (q, k, v))
+    assert not qd.is_contiguous()
+    out = torch.empty(B, S, H, D, device="cuda", dtype=torch.bfloat16).transpose(1, 2)
+    o, lse = attn.fwd(qd, kd, vd, out=out, rebase_threshold=thr)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = ref.attention(to_f64(q), to_f64(k), to_f64(v), 1.0 / np.sqrt(128))
+    compare(to_f64(o.float().cpu()), lse.double().cpu().numpy(), o_ref, lse_ref)
+
+
+def test_packed_qkv_slices():
+    # q, k, v as slices of one packed [B, S, 3, H, D] buffer (strides: S*3*H*D, D, 3*H*D).
+    B, H, S, D = 1, 4, 300, 128
+    g = torch.Generator().manual_seed(41)
+    qkv = torch.randn(B, S, 3, H, D, generator=g).to(torch.bfloat16)
+    q, k, v = (qkv[:, :, j].transpose(1, 2) for j in range(3))
+    qkv_d = qkv.cuda()
+    qd, kd, vd = (qkv_d[:, :, j].transpose(1, 2) for j in range(3))
+    o, lse = attn.fwd(qd, kd, vd)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = ref.attention(to_f64(q), to_f64(k), to_f64(v), 1.0 / np.sqrt(128))
+    compare(to_f64(o.float().cpu()), lse.double().cpu().numpy(), o_ref, lse_ref)
+
+
 def test_guard_regions_untouched():
     B, H, S, D = 1, 2, 200, 128
     q, k, v = (t.cuda() for t in wl.make_custom(B, H, S, seed=11))
