@@ -28,7 +28,7 @@
 //    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
-// the first 64 columns of S_q. Warp 12 loads, warp 13 owns the TMEM allocation. Every
+// the first 64 columns of S_q. Warp 14 loads, warp 13 owns the TMEM allocation. Every
 // mbarrier wait is bounded (about two seconds); a CTA that
 // gives up records the failure in a device status word, drains its own TMA loads and MMAs,
 // frees its tensor memory and exits.
@@ -53,7 +53,7 @@ constexpr int kTileBytes = kBlock * kHeadDim * 2;  // one 128x128 BF16 tile: 32 
 constexpr int kSliceBytes = kBlock * 128;        // 128 rows x 128 B: one SW128 column of atoms
 constexpr int kStages = 4;                       // K/V ring slots
 constexpr int kThreads = 512;                    // 16 warps
-constexpr int kLoadWarp = 12;
+constexpr int kLoadWarp = 14;
 constexpr int kMmaWarp = 13;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
@@ -290,7 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ping-pong); without the turns both tiles drift into lockstep and the pipe idles while
     // both softmaxes run. Turn barrier kBarTurn + q completes once per group the other
     // leader has issued.
-    const bool leader = (warp & 3) == 0 && lane == 0;
+    // The two leaders and the TMA producer sit on three different SM sub-partitions (warp w
+    // runs on sub-partition w % 4): a softmax warp that shares its sub-partition with the
+    // other Q tile's issuing thread or with the producer runs its exp loop measurably slower,
+    // and the warpgroup waits for its slowest warp.
+    const bool leader = (warp & 3) == q && lane == 0;
     const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
     const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
     constexpr uint32_t kTileUnits = kTileBytes >> 4;            // one 32 KB tile, 16-byte units
