@@ -29,6 +29,12 @@ keys j < S, non-causal, no mask):
     lse_i = m_i + ln l_i          (natural log of sum_j exp(s_ij); the pages do not print
                                    lse, this is the usual FlashAttention convention)
 
+Causal variant (``causal=True``). The pages fix their scope to non-causal attention; the
+causal mask is the usual decoder one, with queries and keys on the same positions 0..S-1:
+query i sees keys j <= i only, i.e. s_ij = -inf for j > i before the softmax, and every max,
+sum and product above runs over j <= i. Row i then equals the non-causal definition applied
+to q_i and the first i + 1 keys and values.
+
 All arithmetic is float64. Inputs are whatever float arrays the caller passes (the tests
 pass the BF16 tensors the GPU reads, widened exactly).
 """
@@ -50,10 +56,14 @@ def _as_heads(x: np.ndarray) -> np.ndarray:
     return x.reshape((-1,) + x.shape[-2:])
 
 
-def _softmax_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
+def _softmax_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                  row_ids=None):
     """Exact softmax attention for a block of query rows of one head ([B200-attn] Ch. 1 §ii,
-    with the max trick of Ch. 1 §B)."""
+    with the max trick of Ch. 1 §B). With ``row_ids`` (the rows' positions) the causal mask
+    hides keys j > row_id."""
     s = scale * (q_rows @ k.T)                 # scores, [rows, S]
+    if row_ids is not None:
+        s = np.where(np.arange(k.shape[0])[None, :] > np.asarray(row_ids)[:, None], -np.inf, s)
     m = s.max(axis=1, keepdims=True)           # row max
     e = np.exp(s - m)                          # unnormalised probabilities
     l = e.sum(axis=1, keepdims=True)           # row sum
@@ -62,7 +72,7 @@ def _softmax_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float
     return o, lse
 
 
-def attention(q, k, v, scale: float, row_block: int = 512):
+def attention(q, k, v, scale: float, row_block: int = 512, causal: bool = False):
     """O and lse for every row of every head. q, k, v: [..., S, D]; returns
     (o [..., S, D], lse [..., S]) in float64."""
     qh, kh, vh = _as_heads(q), _as_heads(k), _as_heads(v)
@@ -72,12 +82,13 @@ def attention(q, k, v, scale: float, row_block: int = 512):
     for h in range(n):
         for r0 in range(0, S, row_block):
             r1 = min(S, r0 + row_block)
-            o[h, r0:r1], lse[h, r0:r1] = _softmax_rows(qh[h, r0:r1], kh[h], vh[h], scale)
+            ids = np.arange(r0, r1) if causal else None
+            o[h, r0:r1], lse[h, r0:r1] = _softmax_rows(qh[h, r0:r1], kh[h], vh[h], scale, ids)
     lead = np.asarray(q).shape[:-2]
     return o.reshape(lead + (S, vh.shape[-1])), lse.reshape(lead + (S,))
 
 
-def attention_rows(q, k, v, scale: float, rows, row_block: int = 512):
+def attention_rows(q, k, v, scale: float, rows, row_block: int = 512, causal: bool = False):
     """O and lse for a subset of query rows (the same rows in every head). Rows are
     independent in the definition, so this is exact for those rows."""
     rows = np.asarray(rows, dtype=np.int64)
@@ -89,7 +100,7 @@ def attention_rows(q, k, v, scale: float, rows, row_block: int = 512):
         for r0 in range(0, rows.size, row_block):
             sel = rows[r0:r0 + row_block]
             o[h, r0:r0 + sel.size], lse[h, r0:r0 + sel.size] = _softmax_rows(
-                qh[h, sel], kh[h], vh[h], scale)
+                qh[h, sel], kh[h], vh[h], scale, sel if causal else None)
     lead = np.asarray(q).shape[:-2]
     return o.reshape(lead + (rows.size, vh.shape[-1])), lse.reshape(lead + (rows.size,))
 
@@ -104,7 +115,7 @@ def probabilities(q, k, scale: float):
     return p.reshape(lead + p.shape[1:])
 
 
-def attention_bruteforce(q, k, v, scale: float):
+def attention_bruteforce(q, k, v, scale: float, causal: bool = False):
     """The definition with pure-Python loops and math.exp, for tiny inputs only."""
     qh, kh, vh = _as_heads(q).tolist(), _as_heads(k).tolist(), _as_heads(v).tolist()
     o_all, lse_all = [], []
@@ -113,7 +124,8 @@ def attention_bruteforce(q, k, v, scale: float):
         o_h, lse_h = [], []
         for i in range(S):
             scores = []
-            for j in range(S):
+            keys = range(i + 1) if causal else range(S)
+            for j in keys:
                 acc = 0.0
                 for d in range(len(qq[i])):
                     acc += qq[i][d] * kk[j][d]
@@ -124,7 +136,7 @@ def attention_bruteforce(q, k, v, scale: float):
             row = []
             for d in range(len(vv[0])):
                 acc = 0.0
-                for j in range(S):
+                for j in keys:
                     acc += w[j] * vv[j][d]
                 row.append(acc / tot)
             o_h.append(row)
@@ -138,7 +150,7 @@ def attention_bruteforce(q, k, v, scale: float):
 
 
 def online_softmax_attention(q, k, v, scale: float, tile: int = 128,
-                             rebase_threshold: float = 8.0):
+                             rebase_threshold: float = 8.0, causal: bool = False):
     """The pages' online-softmax recurrence, one K/V tile at a time, in fp64.
 
     Follows [B200-attn] Ch. 1 §B (state update per K/V tile), Ch. 8 (base-2 exponent with
@@ -147,7 +159,9 @@ def online_softmax_attention(q, k, v, scale: float, tile: int = 128,
     ``rebase_threshold`` base-2 units; threshold 0 rebases whenever the max grows). Keys
     past S in the last tile are excluded (they contribute nothing). Returns (o, lse) like
     :func:`attention`; the pages' claim is that the result does not depend on the
-    threshold, which the tests check against the plain definition.
+    threshold, which the tests check against the plain definition. With ``causal`` the
+    scores of keys j > i are -inf before the tile max, so a tile entirely in row i's future
+    leaves that row's state unchanged.
     """
     qh, kh, vh = _as_heads(q), _as_heads(k), _as_heads(v)
     n, S, _ = qh.shape
@@ -161,6 +175,8 @@ def online_softmax_attention(q, k, v, scale: float, tile: int = 128,
         for j0 in range(0, S, tile):
             j1 = min(S, j0 + tile)
             s_raw = qh[h] @ kh[h, j0:j1].T    # this tile's raw scores
+            if causal:
+                s_raw = np.where(np.arange(j0, j1)[None, :] > np.arange(S)[:, None], -np.inf, s_raw)
             tile_max = s_raw.max(axis=1) * scale_log2
             candidate = np.maximum(kept, tile_max)
             first = np.isneginf(kept)

@@ -230,3 +230,75 @@ def test_bf16_output_cannot_always_be_within_1p5e2():
     assert torch.tensor([4.0, 4.03125]).to(torch.bfloat16).view(torch.int16).tolist() == [0x4080, 0x4081]
     assert torch.tensor([4.015625]).to(torch.bfloat16).item() in (4.0, 4.03125)
     assert min(abs(4.015625 - 4.0), abs(4.015625 - 4.03125)) == 0.015625 > 1.5e-2
+
+
+# --- 8. the causal variant (not on the pages: the usual decoder mask, key j visible to
+#        query i iff j <= i) ----------------------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 2, 3, 17, 32])
+def test_causal_matches_bruteforce(S):
+    q, k, v = _rand(2, S, 5, gain=2.0), _rand(2, S, 5, gain=2.0), _rand(2, S, 5)
+    o, lse = ref.attention(q, k, v, 0.6, row_block=7, causal=True)
+    ob, lseb = ref.attention_bruteforce(q, k, v, 0.6, causal=True)
+    assert np.max(np.abs(o - ob)) < 1e-12 and np.max(np.abs(lse - lseb)) < 1e-12
+
+
+def test_causal_first_row_is_first_value():
+    # Row 0 sees key 0 only: O = V[0], lse = s_00.
+    q, k, v = _rand(3, 40, 8), _rand(3, 40, 8), _rand(3, 40, 8)
+    o, lse = ref.attention(q, k, v, 0.35, causal=True)
+    assert np.max(np.abs(o[:, 0] - v[:, 0])) < 1e-14
+    assert np.max(np.abs(lse[:, 0] - 0.35 * np.einsum("nd,nd->n", q[:, 0], k[:, 0]))) < 1e-14
+
+
+def test_causal_row_is_plain_attention_over_its_prefix():
+    # Row i equals the non-causal definition on q_i and the first i + 1 keys and values,
+    # and the last row sees every key.
+    q, k, v = _rand(2, 70, 6, gain=2.0), _rand(2, 70, 6, gain=2.0), _rand(2, 70, 6)
+    o, lse = ref.attention(q, k, v, 0.4, row_block=16, causal=True)
+    for i in (1, 5, 31, 32, 69):
+        op, lp = ref.attention(q[:, : i + 1], k[:, : i + 1], v[:, : i + 1], 0.4)
+        assert np.max(np.abs(o[:, i] - op[:, i])) < 1e-13 and np.max(np.abs(lse[:, i] - lp[:, i])) < 1e-13
+    of, lf = ref.attention(q, k, v, 0.4)
+    assert np.max(np.abs(o[:, -1] - of[:, -1])) < 1e-13 and np.max(np.abs(lse[:, -1] - lf[:, -1])) < 1e-13
+
+
+def test_causal_ignores_the_future():
+    # Changing keys and values after position t leaves rows 0..t unchanged.
+    q, k, v = _rand(1, 50, 4), _rand(1, 50, 4), _rand(1, 50, 4)
+    o, lse = ref.attention(q, k, v, 0.5, causal=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 21:] = _rand(1, 29, 4, gain=5.0)
+    v2[:, 21:] = _rand(1, 29, 4, gain=5.0)
+    o2, lse2 = ref.attention(q, k2, v2, 0.5, causal=True)
+    assert np.array_equal(o[:, :21], o2[:, :21]) and np.array_equal(lse[:, :21], lse2[:, :21])
+    assert np.max(np.abs(o[:, 21:] - o2[:, 21:])) > 1e-3
+
+
+def test_causal_rows_subset_is_exact():
+    q, k, v = _rand(2, 300, 8), _rand(2, 300, 8), _rand(2, 300, 8)
+    rows = np.array([0, 1, 127, 128, 255, 299])
+    o, lse = ref.attention(q, k, v, 0.3, causal=True)
+    os_, ls_ = ref.attention_rows(q, k, v, 0.3, rows, row_block=4, causal=True)
+    assert np.max(np.abs(o[:, rows] - os_)) < 1e-14 and np.max(np.abs(lse[:, rows] - ls_)) < 1e-14
+
+
+def test_causal_matches_torch_sdpa_fp64():
+    q, k, v = (torch.from_numpy(_rand(2, 3, 45, 16, gain=1.5)) for _ in range(3))
+    o, lse = ref.attention(q.numpy(), k.numpy(), v.numpy(), 0.2, causal=True)
+    o_t = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=0.2)
+    mask = torch.ones(45, 45, dtype=torch.bool).tril()
+    s = torch.where(mask, 0.2 * q @ k.transpose(-1, -2), torch.tensor(-math.inf, dtype=torch.float64))
+    assert np.max(np.abs(o - o_t.numpy())) < 1e-10
+    assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).numpy())) < 1e-10
+
+
+@pytest.mark.parametrize("threshold", [0.0, 8.0])
+@pytest.mark.parametrize("S,tile", [(300, 128), (97, 16), (256, 128)])
+def test_causal_online_recurrence(threshold, S, tile):
+    # Tiles wholly in a row's future leave its state alone; the recurrence still equals the
+    # definition.
+    q, k, v = _rand(2, S, 8, gain=2.5), _rand(2, S, 8, gain=2.5), _rand(2, S, 8)
+    o, lse = ref.attention(q, k, v, 0.3, causal=True)
+    oo, lo = ref.online_softmax_attention(q, k, v, 0.3, tile=tile, rebase_threshold=threshold, causal=True)
+    assert np.max(np.abs(o - oo)) < 1e-12 and np.max(np.abs(lse - lo)) < 1e-12
