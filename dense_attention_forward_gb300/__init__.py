@@ -30,7 +30,7 @@ def _check(name, t, shape=None):
 
 
 def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True,
-        stream=None, rebase_threshold: int = 0):
+        stream=None, rebase_threshold: int = 0, causal: bool = False):
     """Attention forward on the current CUDA stream (or `stream`).
 
     q, k, v: bfloat16 CUDA tensors shaped [B, H, S, 128] with a contiguous last dimension;
@@ -39,6 +39,7 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     Returns (o, lse) with o bfloat16 [B, H, S, 128] (contiguous unless `out` is given) and
     lse float32 [B, H, S] (natural log), or (o, None) when return_lse is False.
     rebase_threshold (0 or 8) selects the online-softmax rebase rule (see attn_fwd_ex).
+    causal=True applies the causal mask (query i sees keys j <= i; see attn_fwd_causal).
     """
     import torch
     _check("q", q)
@@ -64,14 +65,14 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
         stream = torch.cuda.current_stream(q.device)
     lse_ptr = lse.data_ptr() if lse is not None else None
     with torch.cuda.device(q.device):
-        if all(t.is_contiguous() for t in (q, k, v, out)):
+        if not causal and all(t.is_contiguous() for t in (q, k, v, out)):
             st = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
                              B, H, S, D, float(scale), int(rebase_threshold), stream.cuda_stream)
         else:
             st = attn_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
                                   B, H, S, D, float(scale), q.stride()[:3], k.stride()[:3],
                                   v.stride()[:3], out.stride()[:3], int(rebase_threshold),
-                                  stream.cuda_stream)
+                                  int(bool(causal)), stream.cuda_stream)
     if st != 0:
         raise AttnError(st)
     return out, lse

@@ -31,7 +31,11 @@ SIGNATURES = {
                                         ctypes.POINTER(ctypes.c_longlong),
                                         ctypes.POINTER(ctypes.c_longlong),
                                         ctypes.POINTER(ctypes.c_longlong), ctypes.c_int,
-                                        ctypes.c_void_p]),
+                                        ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_causal": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
     "attn_version": (ctypes.c_int, []),
@@ -93,12 +97,12 @@ def attn_fwd_ex(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | N
 
 def attn_fwd_strided(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None, B: int,
                      H: int, S: int, D: int, scale: float, q_strides, k_strides, v_strides,
-                     o_strides, rebase_threshold_log2: int, stream: int | None) -> int:
+                     o_strides, rebase_threshold_log2: int, causal: int, stream: int | None) -> int:
     """Direct call of attn_fwd_strided; each *_strides is (batch, head, seq) in elements."""
     arr = ctypes.c_longlong * 3
     return lib().attn_fwd_strided(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, S, D, scale,
                                   arr(*q_strides), arr(*k_strides), arr(*v_strides),
-                                  arr(*o_strides), rebase_threshold_log2, stream)
+                                  arr(*o_strides), rebase_threshold_log2, causal, stream)
 
 
 def device_status(reset: bool = True) -> int:

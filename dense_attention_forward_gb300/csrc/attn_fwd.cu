@@ -95,6 +95,7 @@ struct Params {
   int H;            // heads (the tensor maps are 4-D: {D, S, H, B})
   int n_kv;         // ceil(S / 128)
   int n_qp;         // ceil(S / 256): CTAs per (b, h)
+  int BH;           // B * H
   float scale_log2; // scale * log2(e)
 };
 
@@ -157,7 +158,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // "skip O rescale"; P can then reach 2^8, and O is normalised by a second row sum over the
 // BF16-rounded P. Otherwise (threshold 0) the kept max is the running max, P <= 1 with the
 // row maximum exactly 1, and one fp32 row sum serves both O and lse.
-template <bool kRebase8>
+// kCausal: query i sees keys j <= i (queries and keys share positions 0..S-1). The CTA of Q
+// tiles 2qp and 2qp+1 walks K/V tiles 0..2qp+1 only; its diagonal tiles are masked per
+// element, and Q tile 2qp runs tile 2qp+1 fully masked (P = 0) so both Q tiles keep the same
+// K/V schedule. CTAs are launched longest first (descending qp, all heads) to shorten the
+// tail of the grid.
+template <bool kRebase8, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -169,11 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qp = blockIdx.x % p.n_qp;
-  const int bh = blockIdx.x / p.n_qp;
+  const int qp = kCausal ? p.n_qp - 1 - static_cast<int>(blockIdx.x) / p.BH
+                         : static_cast<int>(blockIdx.x) % p.n_qp;
+  const int bh = kCausal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / p.n_qp;
   const int hh = bh % p.H, bb = bh / p.H;
   const int q0 = qp * 2 * kBlock;
-  const int n = p.n_kv;
+  const int n = kCausal ? min(p.n_kv, 2 * qp + 2) : p.n_kv;  // K/V tiles this CTA walks
 
   Ctl c;
   c.bar0 = base + kOffBar;
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
     const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
     const float sl2 = p.scale_log2;
-    const int rem = p.S - (n - 1) * kBlock;  // valid keys in the last tile, 1..128
+    const int rem = p.S - (p.n_kv - 1) * kBlock;  // valid keys in the last tile, 1..128
     float m_kept = -INFINITY;                 // kept row max, base-2 units
     float l = 0.f;                            // running row sum that normalises O
     float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
@@ -361,9 +368,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sr[j]);
-      if (i == n - 1 && rem < kBlock) {
+      if (i == p.n_kv - 1 && rem < kBlock) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = (j < rem) ? s[j] : -INFINITY;
+      }
+      if (kCausal && i >= 2 * qp + q) {
+        // Diagonal tile (and, for Q tile 2qp, the tile after it): column j is key
+        // i*128 + j, visible to this row while it is <= the row's position.
+        const int lim = q0 + q * kBlock + row - i * kBlock;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) s[j] = (j <= lim) ? s[j] : -INFINITY;
       }
       float mx[4];
 #pragma unroll
@@ -602,9 +616,13 @@ int prepare_device(int* dev_out) {
     g_dev_state[dev].store(-1, std::memory_order_release);
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
-  if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn_fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -668,9 +686,10 @@ extern "C" {
 static int attn_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                        int S, int D, float scale, const long long* qs, const long long* ks,
                        const long long* vs, const long long* os, int rebase_threshold_log2,
-                       void* stream) {
+                       int causal, void* stream) {
   using namespace gb300;
   if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (D != kHeadDim) return ATTN_ERR_UNSUPPORTED_DIM;
   if (!q || !k || !v || !o || !qs || !ks || !vs || !os) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || S <= 0) return ATTN_ERR_INVALID_ARG;
@@ -717,13 +736,18 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   prm.H = H;
   prm.n_kv = static_cast<int>((S + kBlock - 1) / kBlock);
   prm.n_qp = static_cast<int>(n_qp);
+  prm.BH = static_cast<int>(BH);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   const dim3 grid(static_cast<unsigned>(BH * n_qp));
-  if (rebase_threshold_log2 == 8)
-    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
-  else
-    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  if (rebase_threshold_log2 == 8) {
+    if (causal) attn_fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+    else attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+  } else {
+    if (causal) attn_fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+    else attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+  }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -732,15 +756,21 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 int S, int D, float scale, int rebase_threshold_log2, void* stream) {
   // Contiguous [B, H, S, D]: element strides (H*S*D, S*D, D).
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, 0, stream);
 }
 
 int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int S, int D, float scale, const long long* q_strides, const long long* k_strides,
                      const long long* v_strides, const long long* o_strides, int rebase_threshold_log2,
-                     void* stream) {
+                     int causal, void* stream) {
   return attn_launch(q, k, v, o, lse, B, H, S, D, scale, q_strides, k_strides, v_strides, o_strides,
-                     rebase_threshold_log2, stream);
+                     rebase_threshold_log2, causal, stream);
+}
+
+int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int S, int D, float scale, void* stream) {
+  const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

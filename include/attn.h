@@ -82,6 +82,17 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 void* stream);
 
 /*
+ * attn_fwd_causal -- attn_fwd with the causal mask: query i attends to keys j <= i only
+ * (queries and keys share the positions 0..S-1), so every max, sum and product in the
+ * definition above runs over j <= i. Not on the pages, whose scope is non-causal; this is the
+ * usual decoder mask. The kernel visits only the K/V tiles at or before each Q tile's
+ * diagonal (about half the work of attn_fwd at large S). Arguments, errors and ownership as
+ * attn_fwd.
+ */
+int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int S, int D, float scale, void* stream);
+
+/*
  * attn_fwd_strided -- attn_fwd_ex on strided tensors (no copies): [B, S, H, D], slices of a
  * packed QKV buffer, and so on. The head dimension must be contiguous (unit stride).
  *
@@ -94,13 +105,15 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
  *   Overlap between o / lse and the inputs is checked on the address ranges the strides span.
  *   Contiguous [B, H, S, D] corresponds to strides {H*S*D, S*D, D}; [B, S, H, D] to
  *   {S*H*D, D, H*D}.
+ *   causal  : 0 = dense (attn_fwd_ex), 1 = causal mask (attn_fwd_causal); anything else is
+ *             ATTN_ERR_INVALID_ARG.
  * Other arguments, errors and ownership as attn_fwd_ex.
  */
 int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int H, int S, int D, float scale,
                      const long long* q_strides, const long long* k_strides,
                      const long long* v_strides, const long long* o_strides,
-                     int rebase_threshold_log2, void* stream);
+                     int rebase_threshold_log2, int causal, void* stream);
 
 /* A short, static, human-readable description of a status code. Never NULL. */
 const char* attn_status_string(int status);

@@ -30,8 +30,8 @@ def lib():
 
 
 def test_header_declares_the_boundary():
-    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided",
-                                  "attn_status_string", "attn_version"]
+    assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_causal", "attn_fwd_ex",
+                                  "attn_fwd_strided", "attn_status_string", "attn_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -75,11 +75,11 @@ def test_ex_validates_like_attn_fwd(lib):
     assert lib.attn_fwd_ex(Q, K, V, Q, L, 1, 1, 256, 128, 0.088, 0, None) == 1
 
 
-def strided(lib, qs, ks=None, vs=None, os_=None, B=2, H=3, S=256, q=Q, o=O, lse=L):
+def strided(lib, qs, ks=None, vs=None, os_=None, B=2, H=3, S=256, q=Q, o=O, lse=L, causal=0):
     arr = ctypes.c_longlong * 3
     ks, vs, os_ = ks or qs, vs or qs, os_ or qs
     return lib.attn_fwd_strided(q, K, V, o, lse, B, H, S, 128, 0.088, arr(*qs), arr(*ks), arr(*vs),
-                                arr(*os_), 0, None)
+                                arr(*os_), 0, causal, None)
 
 
 BHSD = (3 * 256 * 128, 256 * 128, 128)
@@ -93,6 +93,8 @@ BSHD = (256 * 3 * 128, 128, 3 * 128)
     (dict(qs=BHSD, os_=(128, 128, 128)), 1),                 # output rows would collide
     (dict(qs=BHSD, os_=(256 * 128, 256 * 128, 128)), 1),     # batch and head overlap in o
     (dict(qs=BSHD, o=Q + 128 * 2), 1),                       # o inside q's span
+    (dict(qs=BHSD, causal=2), 1),                            # causal is 0 or 1
+    (dict(qs=BHSD, causal=-1), 1),
 ])
 def test_strided_argument_errors(lib, kw, expected):
     assert strided(lib, **kw) == expected
@@ -101,7 +103,18 @@ def test_strided_argument_errors(lib, kw, expected):
 def test_strided_null_strides(lib):
     arr = ctypes.c_longlong * 3
     assert lib.attn_fwd_strided(Q, K, V, O, L, 1, 1, 256, 128, 0.088, None, arr(*BHSD), arr(*BHSD),
-                                arr(*BHSD), 0, None) == 1
+                                arr(*BHSD), 0, 0, None) == 1
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(D=64), 2), (dict(q=None), 1), (dict(S=0), 1), (dict(scale=-1.0), 1), (dict(o=O + 2), 3),
+    (dict(o=V), 1),
+])
+def test_causal_argument_errors(lib, kw, expected):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, S=256, D=128, scale=0.088)
+    a.update(kw)
+    assert lib.attn_fwd_causal(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["S"], a["D"],
+                               a["scale"], None) == expected
 
 
 def test_no_device_is_reported(lib):
@@ -109,6 +122,7 @@ def test_no_device_is_reported(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call(lib) == 4  # ATTN_ERR_UNSUPPORTED_DEVICE, nothing launched
+    assert lib.attn_fwd_causal(Q, K, V, O, L, 1, 1, 256, 128, 0.088, None) == 4
     word = ctypes.c_uint(7)
     assert lib.attn_device_status(ctypes.byref(word), 0) == 4
     assert lib.attn_device_status(None, 0) == 1
