@@ -171,16 +171,16 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def time_gpu(attn, torch, w, q, k, v, o, lse, steps, warmup, flush, stream):
+def time_gpu(attn, torch, w, q, k, v, o, lse, steps, warmup, flush, stream, causal=False):
     for _ in range(warmup):
-        attn.fwd(q, k, v, w.scale, out=o, lse=lse)
+        attn.fwd(q, k, v, w.scale, out=o, lse=lse, causal=causal)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
         flush.add_(1)  # write > L2 between timed calls
         starts[i].record(stream)
-        attn.fwd(q, k, v, w.scale, out=o, lse=lse)
+        attn.fwd(q, k, v, w.scale, out=o, lse=lse, causal=causal)
         ends[i].record(stream)
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -274,6 +274,17 @@ def run_gpu(args, w):
             sweep[name] = {"workload": ws.label(), "ms": round(ms, 4),
                            "tflops": round(ws.flops / (ms * 1e-3) / 1e12, 1)}
             del qs, ks, vs, os_, ls_
+        # The causal variant (query i sees keys j <= i), FLOPs counted as 2*B*H*S^2*D.
+        for name in args.causal_sweep:
+            ws = wl.ALL[name]
+            qs, ks, vs = (t.to(dev) for t in wl.make_qkv(ws))
+            os_, ls_ = torch.empty_like(qs), torch.empty((ws.B, ws.H, ws.S), device=dev)
+            ts = time_gpu(attn, torch, ws, qs, ks, vs, os_, ls_, args.sweep_steps, 3, flush, stream,
+                          causal=True)
+            ms = sum(ts) / len(ts)
+            sweep[name + "_causal"] = {"workload": ws.label() + " causal", "ms": round(ms, 4),
+                                       "tflops": round(ws.flops / 2 / (ms * 1e-3) / 1e12, 1)}
+            del qs, ks, vs, os_, ls_
         status |= attn.device_status(reset=True)
 
     if rank != 0:
@@ -329,6 +340,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="s4k", choices=sorted(wl.ALL))
     ap.add_argument("--sweep", nargs="*", default=["s8k", "s16k", "ragged"])
+    ap.add_argument("--causal-sweep", nargs="*", default=["s4k", "s8k", "s16k"])
     ap.add_argument("--sweep-steps", type=int, default=100)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
