@@ -326,6 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma8_bf16_ss<0>(tSq, a, b, kIdescQK);
     };
+    // The same, handing the turn to the other leader after the seventh MMA: the other
+    // leader sees the arrival a couple of hundred cycles later, by which time the last MMA
+    // and the commits are queued, so its first MMA follows without a gap in the tensor pipe.
+    auto issue_qk_hand_over = [&](uint32_t k_slot) {
+      const uint64_t b0 = dk + k_slot * kTileUnits;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss(tSq, dq + off, b0 + off, kIdescQK, kk > 0 ? 1u : 0u);
+        if (kk == 6) {
+          tc_fence_before();
+          mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
+        }
+      }
+    };
     // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
     // V rows [16kk, 16kk+16) (2048 B further per step).
     auto issue_pv = [&](uint32_t v_slot, bool first) {
@@ -459,16 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(static_cast<uint32_t>(tv % kStages), i == 0);
           mma_commit(c.bar(kBarKVEmpty + tv % kStages));
           if (more) {
-            issue_qk(static_cast<uint32_t>(tk % kStages));
+            issue_qk_hand_over(static_cast<uint32_t>(tk % kStages));  // hands the turn over
             mma_commit(c.bar(kBarSFull + q));
             mma_commit(c.bar(kBarKVEmpty + tk % kStages));
           } else {
             mma_commit(c.bar(kBarOFull + q));
-          }
-          // Hand the turn over (leader 1's last group has no successor).
-          if (q == 0 || more) {
-            tc_fence_before();
-            mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
+            // Leader 0's last group still hands over; leader 1's has no successor.
+            if (q == 0) {
+              tc_fence_before();
+              mbar_arrive(c.bar(kBarTurn + 1));
+            }
           }
         }
       }
