@@ -24,8 +24,10 @@
 //    conversions and byte permutes run per element: on this part scalar FP32 and IMAD work
 //    in other warps slows the tensor pipe.
 //  * Correction (Ch. 11, Ch. 12): 4 warps shared by both Q tiles rescale O in tensor memory
-//    when any row of their 32 rebased, then run the epilogue (O / l -> BF16 -> SW128 shared
-//    memory -> TMA store). lse = (m + log2 l) * ln 2 is written by the softmax threads.
+//    when any row of their 32 rebased.
+//  * Epilogue (Ch. 1): each softmax warp turns its 32 rows of O / l into BF16, stages them
+//    SW128 in the dead Q_q buffer and TMA-stores them (32-row boxes, no cross-warp barrier);
+//    lse = (m + log2 l) * ln 2 is written by the same threads.
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
 // the first 64 columns of S_q. Warp 14 loads, warp 13 owns the TMEM allocation. Every
@@ -70,15 +72,13 @@ constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_q in TMEM (MMA commi
 constexpr int kBarOSafe = kBarSFull + 2;           // [2] O_q rescaled or left as is (4 correction warps)
 constexpr int kBarOFull = kBarOSafe + 2;           // [2] last PV_q done (MMA commit)
 constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
-constexpr int kBarLReady = kBarStats + 2;          // [2] final row sums published (4 warps)
-constexpr int kBarMmaDone = kBarLReady + 2;        // [2] drain after a failure (one per issuing thread)
+constexpr int kBarMmaDone = kBarStats + 2;         // [2] drain after a failure (one per issuing thread)
 constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q tile q (the other leader)
 constexpr int kNumBars = kBarTurn + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffAlpha = (kOffAbort + 4 + 15) & ~15;      // float[2][128]
-constexpr int kOffLFinal = kOffAlpha + 2 * kBlock * 4;     // float[2][128]
-constexpr int kSmemUsed = kOffLFinal + 2 * kBlock * 4;
+constexpr int kSmemUsed = kOffAlpha + 2 * kBlock * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for the 1024-byte alignment
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -187,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   float* const alpha_sm = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* const lfin_sm = reinterpret_cast<float*>(smem + kOffLFinal);
   const uint32_t q_smem = base + kOffQ;
   const uint32_t kv_smem = base + kOffKV;
 
@@ -203,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(kBarOSafe + q), 4);
       mbar_init(c.bar(kBarOFull + q), 1);
       mbar_init(c.bar(kBarStats + q), 4);
-      mbar_init(c.bar(kBarLReady + q), 4);
     }
     mbar_init(c.bar(kBarMmaDone + 0), 1);
     mbar_init(c.bar(kBarMmaDone + 1), 1);
@@ -223,10 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // Register split (warpgroup granularity, set at the top of each role's branch so the
-  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 72 +
-  // load/MMA WG 56 = 65536 = 512 threads x 128 registers at launch.
+  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 64 +
+  // load/TMEM WG 64 = 65536 = 512 threads x 128 registers at launch.
   if (warp >= 12) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
   }
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------------ TMA producer
@@ -495,16 +493,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_slow(c, kBarMmaDone + q, 0, kRoleSoftmax, false, kDrainLimitNs);
     }
     __syncwarp();
-    if (ok) {
-      lfin_sm[q * kBlock + row] = l;
-      warp_arrive(c, kBarLReady + q, lane);
+    // epilogue: O / l -> BF16 -> SW128 staging in the dead Q_q buffer -> one TMA store of
+    // this warp's 32 rows (no cross-warp barrier; the two Q tiles finish independently).
+    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the leader
+    // issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
+    if (ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax)) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256u + q * 128u;
+      uint32_t o[128];
+      tmem_ld32_x128_sync(tO, o);
+      const uint32_t stage = q_smem + q * kTileBytes;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunk ch = columns 8ch..8ch+7
+        uint32_t w4[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          w4[t] = pack_bf16x2(__uint_as_float(o[8 * ch + 2 * t]) * inv_l,
+                              __uint_as_float(o[8 * ch + 2 * t + 1]) * inv_l);
+        const uint32_t addr = stage + (ch >> 3) * kSliceBytes + row * 128 +
+                              (static_cast<uint32_t>((ch & 7) ^ (row & 7)) << 4);
+        st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int r0 = q0 + q * kBlock + (warp & 3) * 32;
+      if (lane == 0 && r0 < p.S) {
+        const uint32_t wst = stage + (warp & 3) * 32 * 128;
+        tma_store_4d(&tm_o, wst, 0, r0, hh, bb);
+        tma_store_4d(&tm_o, wst + kSliceBytes, 64, r0, hh, bb);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+      __syncwarp();
       const int grow = q0 + q * kBlock + row;
       if (p.lse != nullptr && grow < p.S)
         p.lse[static_cast<size_t>(bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
     }
   } else if (warp < 12) {
-    // ------------------------------------------------------------------ correction + epilogue
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+    // ------------------------------------------------------------------ correction
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
@@ -538,39 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_arrive(c, kBarOSafe + q, lane);
       }
     }
-    // epilogue: O / l -> BF16 -> SW128 staging in the dead Q buffer -> TMA store
-    for (int q = 0; q < 2 && ok; ++q) {
-      if (!wait_bar_warp(c, kBarLReady + q, 0, kRoleCorrection)) { ok = false; break; }
-      if (!wait_bar_warp(c, kBarOFull + q, 0, kRoleCorrection)) { ok = false; break; }
-      tc_fence_after();
-      const float inv_l = 1.0f / lfin_sm[q * kBlock + row];
-      const uint32_t stage = q_smem + q * kTileBytes;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32_x32_sync(tO[q] + cc * 32, o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int chunk = cc * 4 + t;  // 16-byte chunk of the 256-byte row, 0..15
-          const uint32_t addr = stage + (chunk >> 3) * kSliceBytes + row * 128 +
-                                (static_cast<uint32_t>((chunk & 7) ^ (row & 7)) << 4);
-          st_shared_v4(addr, pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (warp == 8 && lane == 0 && q0 + q * kBlock < p.S) {
-        tma_store_4d(&tm_o, stage, 0, q0 + q * kBlock, hh, bb);
-        tma_store_4d(&tm_o, stage + kSliceBytes, 64, q0 + q * kBlock, hh, bb);
-        tma_store_commit();
-      }
-    }
-    if (warp == 8 && lane == 0) tma_store_wait_read_all();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -647,13 +642,15 @@ int prepare_device(int* dev_out) {
 }
 
 // A BF16 [B, H, S, D] tensor with element strides (sb, sh, ss) and unit stride along D, as a
-// 4-D tensor map {D, S, H, B}; 64x128 boxes, 128-byte swizzle, zero fill past S.
-bool encode_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, const long long (&st)[3]) {
+// 4-D tensor map {D, S, H, B}; 64 x box_rows boxes (128 for loads, 32 for the per-warp
+// output stores), 128-byte swizzle, zero fill past S.
+bool encode_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, const long long (&st)[3],
+               int box_rows = kBlock) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
                                  static_cast<cuuint64_t>(st[0]) * 2};
-  const cuuint32_t box[4] = {64, kBlock, 1, 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -742,7 +739,7 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
 
   CUtensorMap tq, tk, tv, to;
   if (!encode_4d(&tq, q, B, H, S, st[0]) || !encode_4d(&tk, k, B, H, S, st[1]) ||
-      !encode_4d(&tv, v, B, H, S, st[2]) || !encode_4d(&to, o, B, H, S, st[3]))
+      !encode_4d(&tv, v, B, H, S, st[2]) || !encode_4d(&to, o, B, H, S, st[3], 32))
     return ATTN_ERR_LAUNCH;
 
   Params prm;
