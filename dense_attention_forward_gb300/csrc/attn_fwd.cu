@@ -8,8 +8,9 @@
 //    (batch, head) and walks every 128-key K/V tile of that head; each K/V tile loaded into
 //    shared memory serves both Q tiles.
 //  * Loads (Ch. 3, Ch. 6): one TMA warp streams K and V as separate tokens through a
-//    kStages-slot ring of 32 KB SW128 slots; a slot is refilled once its last consumer (the
-//    second Q tile's QK for K, its PV for V) has committed.
+//    kStages-slot ring of 32 KB SW128 slots; a slot is refilled once the second Q tile's
+//    S-full commit that follows its last consumer (that tile's QK for K, its PV for V) has
+//    arrived, so no MMA commit is spent on freeing slots.
 //  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 5, Ch. 7): tcgen05.mma M128 N128 K16, S_q = Q_q K^T (both
 //    K-major SW128 in shared memory) and O_q += P_q V (P from tensor memory, V MN-major
 //    SW128). Each softmax warpgroup's first thread issues its own Q tile's MMAs, PV_q(i) then
@@ -67,8 +68,7 @@ constexpr int kOffBar = kOffKV + kStages * kTileBytes;     // mbarriers
 // barrier indices
 constexpr int kBarQFull = 0;                       // [2] Q_q landed (TMA bytes)
 constexpr int kBarKVFull = 2;                      // [kStages] token landed (TMA bytes)
-constexpr int kBarKVEmpty = kBarKVFull + kStages;  // [kStages] token consumed: one MMA commit per Q tile
-constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2] S_q in TMEM (MMA commit)
+constexpr int kBarSFull = kBarKVFull + kStages;    // [2] S_q in TMEM (MMA commit); S_1 also frees K/V slots
 constexpr int kBarOSafe = kBarSFull + 2;           // [2] O_q rescaled or left as is (4 correction warps)
 constexpr int kBarOFull = kBarOSafe + 2;           // [2] last PV_q done (MMA commit)
 constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
@@ -193,10 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarQFull + 0), 1);
     mbar_init(c.bar(kBarQFull + 1), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(c.bar(kBarKVFull + s), 1);
-      mbar_init(c.bar(kBarKVEmpty + s), 2);
-    }
+    for (int s = 0; s < kStages; ++s) mbar_init(c.bar(kBarKVFull + s), 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(c.bar(kBarSFull + q), 1);
       mbar_init(c.bar(kBarOSafe + q), 4);
@@ -247,10 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;
       int s = 0;
-      uint32_t empty_phase = 1;  // first pass over the ring: slots start free
       for (int t = 0; t < 2 * n; ++t) {
         if (t >= kStages) {
-          if (!wait_bar(c, kBarKVEmpty + s, empty_phase, kRoleLoad)) { ok = false; break; }
+          // The slot's previous token t-4 is free once Q tile 1's QK that follows its last
+          // use has finished: K(j) after QK_1(j) (S_1(j) full), V(j) after PV_1(j), which
+          // precedes QK_1(j+1) (S_1(j+1) full). The tensor pipe runs MMAs in issue order and
+          // Q tile 1's group starts after Q tile 0's, so both tiles' uses are done then.
+          // The producer is never more than one phase of S_1 behind (phase ph + 2 needs K(ph +
+          // 2), a later token), so the parity wait is unambiguous.
+          const int prev = t - kStages;
+          const int ph = (prev & 1) ? (prev - 1) / 2 + 1 : prev / 2;
+          if (!wait_bar(c, kBarSFull + 1, static_cast<uint32_t>(ph & 1), kRoleLoad)) { ok = false; break; }
         }
         const uint32_t bar = c.bar(kBarKVFull + s);
         const uint32_t dst = kv_smem + s * kTileBytes;
@@ -261,10 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
         issued = t + 1;
         if (t == 0) load_q(1);
-        if (++s == kStages) {
-          s = 0;
-          empty_phase ^= 1u;
-        }
+        if (++s == kStages) s = 0;
       }
       if (!ok) {
         // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
@@ -324,16 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma8_bf16_ss<0>(tSq, a, b, kIdescQK);
     };
-    // The same, handing the turn to the other leader after the seventh MMA: the other
-    // leader sees the arrival a couple of hundred cycles later, by which time the last MMA
-    // and the commits are queued, so its first MMA follows without a gap in the tensor pipe.
+    // The same, handing the turn to the other leader right after the eighth MMA, before the
+    // commit: the other leader sees the arrival a couple of hundred cycles later, so its
+    // first MMA follows without a gap in the tensor pipe, and every MMA of this group is
+    // queued ahead of the other leader's (the producer relies on that order, see below).
     auto issue_qk_hand_over = [&](uint32_t k_slot) {
       const uint64_t b0 = dk + k_slot * kTileUnits;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
         mma_bf16_ss(tSq, dq + off, b0 + off, kIdescQK, kk > 0 ? 1u : 0u);
-        if (kk == 6) {
+        if (kk == 7) {
           tc_fence_before();
           mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
         }
@@ -364,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_qk(0);
         mma_commit(c.bar(kBarSFull + q));
-        mma_commit(c.bar(kBarKVEmpty + 0));
         tc_fence_before();
         mbar_arrive(c.bar(kBarTurn + (q ^ 1)));  // G_q(0) issued
       }
@@ -470,11 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           issue_pv(static_cast<uint32_t>(tv % kStages), i == 0);
-          mma_commit(c.bar(kBarKVEmpty + tv % kStages));
           if (more) {
             issue_qk_hand_over(static_cast<uint32_t>(tk % kStages));  // hands the turn over
             mma_commit(c.bar(kBarSFull + q));
-            mma_commit(c.bar(kBarKVEmpty + tk % kStages));
           } else {
             mma_commit(c.bar(kBarOFull + q));
             // Leader 0's last group still hands over; leader 1's has no successor.
