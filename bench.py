@@ -118,6 +118,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's time: every rank passes its own, every rank gets the maximum."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job TFLOPS: every rank's work over the slowest rank's time (weak scaling)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def time_oracle(w: wl.Workload, q, k, v, budget_s: float, min_chunks: int = 1):
     """Time the oracle on row chunks (all heads) until `budget_s` has elapsed. Returns
     (TFLOPS, seconds, rows_per_head, cores)."""
@@ -220,11 +235,8 @@ def run_gpu(args, w):
         barrier()
         t_wall = time.perf_counter() - t_wall0
     kern_ms = sum(times) / len(times)
-    if dist is not None:
-        t = torch.tensor([kern_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kern_ms = float(t.item())
-    value = world * w.flops / (kern_ms * 1e-3) / 1e12
+    kern_ms = max_over_ranks(kern_ms, dist, dev)
+    value = job_throughput(w.flops, kern_ms, world)
     status = attn.device_status(reset=True)
 
     # ---- end to end: pinned host -> device, attn_fwd, device -> pinned host, every step.
@@ -278,11 +290,8 @@ def run_gpu(args, w):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_throughput(w.flops, e2e_ms, world)
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
