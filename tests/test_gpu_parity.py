@@ -166,3 +166,21 @@ def test_gpu_argument_errors():
 def test_no_wait_gave_up():
     torch.cuda.synchronize()
     assert attn.device_status(reset=False) == 0
+
+
+def test_many_heads_full():
+    # 256 (b, h) pairs x 2 CTAs: more CTAs than SMs, several waves, ragged S.
+    q, k, v = wl.make_custom(4, 64, 300, seed=51)
+    full_parity(q, k, v, 1.0 / np.sqrt(128))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled(causal):
+    # S = 65536 + 77: 514 K/V tiles per CTA, rows sampled at the start, middle and tail.
+    B, H, S = 1, 2, 65536 + 77
+    q, k, v = wl.make_custom(B, H, S, seed=61)
+    o_gpu, lse_gpu = run_gpu(q, k, v, 1.0 / np.sqrt(128), 0, causal=causal)
+    rng = np.random.default_rng(61)
+    rows = np.array(sorted(set(range(0, 40)) | set(range(S - 300, S)) | set(rng.integers(0, S, 40).tolist())))
+    o_ref, lse_ref = ref.attention_rows(to_f64(q), to_f64(k), to_f64(v), 1.0 / np.sqrt(128), rows, causal=causal)
+    compare(o_gpu[..., rows, :], lse_gpu[..., rows], o_ref, lse_ref)
