@@ -18,12 +18,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -67,41 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe of phase `parity`. Its result is scoreboarded like a load, so a thread
-// can issue it, go on issuing independent instructions, and look at the result later.
-__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok;
-}
-
-// Three non-blocking probes in one block: their latencies overlap. Bit i of the result is
-// set if phase par_i of barrier bar_i had completed.
-__device__ __forceinline__ uint32_t mbar_probe3(uint32_t bar0, uint32_t par0, uint32_t bar1,
-                                                uint32_t par1, uint32_t bar2, uint32_t par2) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred q0, q1, q2;\n\t.reg .b32 t0, t1, t2;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
-      "selp.u32 t0, 1, 0, q0;\n\t"
-      "selp.u32 t1, 2, 0, q1;\n\t"
-      "selp.u32 t2, 4, 0, q2;\n\t"
-      "or.b32 t0, t0, t1;\n\t"
-      "or.b32 %0, t0, t2;\n}\n"
-      : "=r"(r)
-      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1), "r"(bar2), "r"(par2)
-      : "memory");
-  return r;
-}
-
 // Four probes in one block (bits 0-3).
 __device__ __forceinline__ uint32_t mbar_probe4(uint32_t bar0, uint32_t par0, uint32_t bar1,
                                                 uint32_t par1, uint32_t bar2, uint32_t par2,
@@ -143,17 +102,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Same, with an L2 cache-policy hint (createpolicy result).
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int c0, int c1, int c2,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
 // 4-D tiled load with an L2 cache-policy hint (coordinates innermost first).
 __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                  int c0, int c1, int c2, int c3, uint64_t policy) {
@@ -186,16 +134,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
-// 3-D tiled store from shared memory (rows outside the tensor are clipped by the hardware).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -203,10 +141,6 @@ __device__ __forceinline__ void tma_store_commit() {
 // Wait until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void tma_store_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------
@@ -236,10 +170,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -266,35 +196,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same two forms with each descriptor passed as its (low, high) 32-bit words and the
-// accumulate flag as a compile-time constant: the issuing thread then spends one integer add
-// per operand between consecutive MMAs. (A tcgen05.mma is not accepted until the tensor core
-// can take it, so instructions between two MMAs add directly to the MMA period.)
-template <int kAccumulate>
-__device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                              uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "mov.b64 da, {%1, %2};\n\t"
-      "mov.b64 db, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAccumulate)
-      : "memory");
-}
-
-template <int kAccumulate>
-__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                              uint32_t b_hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAccumulate)
       : "memory");
 }
 
@@ -343,62 +244,6 @@ __device__ __forceinline__ void mma8_bf16_ts(uint32_t d_tmem, const uint32_t (&a
       "r"(idesc), "n"(kAcc0)
       : "memory");
 }
-
-// The same eight-MMA groups, with up to two mbarrier probes issued in the same asm block
-// ahead of the MMAs and their predicates read after them: a probe's result takes a few
-// hundred cycles to come back inside the running kernel, and this way that latency overlaps
-// the MMAs instead of stalling the issuing thread before them. probe[i] receives 1 if phase
-// `parity[i]` of barrier `bar[i]` had completed (bar == 0 with nprobes < 2 skips the second).
-#define GB300_MMA8_BODY(A0, A1, A2, A3, A4, A5, A6, A7)                                      \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A0 ", %12, %20, p0;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A1 ", %13, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A2 ", %14, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A3 ", %15, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A4 ", %16, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A5 ", %17, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A6 ", %18, %20, p1;\n\t"                    \
-  "tcgen05.mma.cta_group::1.kind::f16 [%2], " A7 ", %19, %20, p1;\n\t"
-
-template <int kAcc0>
-__device__ __forceinline__ void mma8_bf16_ss_probe(uint32_t d_tmem, const uint64_t (&a)[8],
-                                                   const uint64_t (&b)[8], uint32_t idesc,
-                                                   uint32_t bar0, uint32_t par0, uint32_t bar1,
-                                                   uint32_t par1, uint32_t& probe0, uint32_t& probe1) {
-  asm volatile(
-      "{\n\t.reg .pred p0, p1, q0, q1;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%22], %23;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%24], %25;\n\t"
-      "setp.ne.b32 p0, %21, 0;\n\t"
-      "setp.eq.u32 p1, %20, %20;\n\t" GB300_MMA8_BODY("%3", "%4", "%5", "%6", "%7", "%8", "%9", "%10")
-      "selp.u32 %0, 1, 0, q0;\n\t"
-      "selp.u32 %1, 1, 0, q1;\n}\n"
-      : "=r"(probe0), "=r"(probe1)
-      : "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]),
-        "l"(a[7]), "n"(0), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
-        "l"(b[6]), "l"(b[7]), "r"(idesc), "n"(kAcc0), "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
-      : "memory");
-}
-
-template <int kAcc0>
-__device__ __forceinline__ void mma8_bf16_ts_probe(uint32_t d_tmem, const uint32_t (&a)[8],
-                                                   const uint64_t (&b)[8], uint32_t idesc,
-                                                   uint32_t bar0, uint32_t par0, uint32_t bar1,
-                                                   uint32_t par1, uint32_t& probe0, uint32_t& probe1) {
-  asm volatile(
-      "{\n\t.reg .pred p0, p1, q0, q1;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%22], %23;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%24], %25;\n\t"
-      "setp.ne.b32 p0, %21, 0;\n\t"
-      "setp.eq.u32 p1, %20, %20;\n\t" GB300_MMA8_BODY("[%3]", "[%4]", "[%5]", "[%6]", "[%7]", "[%8]", "[%9]", "[%10]")
-      "selp.u32 %0, 1, 0, q0;\n\t"
-      "selp.u32 %1, 1, 0, q1;\n}\n"
-      : "=r"(probe0), "=r"(probe1)
-      : "r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
-        "r"(a[7]), "n"(0), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]),
-        "l"(b[6]), "l"(b[7]), "r"(idesc), "n"(kAcc0), "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
-      : "memory");
-}
-#undef GB300_MMA8_BODY
 
 // The two BF16 halves of `pk` as FP32 values, with byte permutes (integer ALU pipe).
 // On this part FMA-pipe instructions issued by other warps (scalar FFMA/FADD/FMUL, IMAD,
