@@ -32,9 +32,13 @@
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
 // the first 64 columns of S_q. Warp 14 loads, warp 13 owns the TMEM allocation. Every
-// mbarrier wait is bounded (about two seconds); a CTA that
-// gives up records the failure in a device status word, drains its own TMA loads and MMAs,
-// frees its tensor memory and exits.
+// mbarrier wait is bounded (about two seconds); a CTA that gives up records the failure in a
+// device status word, drains its own TMA loads and MMAs, frees its tensor memory and exits.
+// The only other barriers are the CTA-wide ones at entry and exit, and each softmax
+// warpgroup's per-tile named barrier: a warp that gives up records the iteration in shared
+// memory before it joins that barrier, and the other three leave at the same iteration.
+// attn_fwd_withhold runs this path on purpose: its producer skips one K/V token, so the waits
+// on that token run out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -77,7 +81,8 @@ constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q ti
 constexpr int kNumBars = kBarTurn + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kOffAlpha = (kOffAbort + 4 + 15) & ~15;      // float[2][128]
+constexpr int kOffFail = kOffAbort + 4;                    // int[2]: iteration + 1 a softmax warp gave up
+constexpr int kOffAlpha = (kOffFail + 8 + 15) & ~15;       // float[2][128]
 constexpr int kSmemUsed = kOffAlpha + 2 * kBlock * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for the 1024-byte alignment
 
@@ -97,6 +102,7 @@ struct Params {
   int n_qp;         // ceil(S / 256): CTAs per (b, h)
   int BH;           // B * H
   float scale_log2; // scale * log2(e)
+  int withhold;     // K/V token the producer never loads (bounded-wait test hook), -1: none
 };
 
 struct Ctl {
@@ -205,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(c.bar(kBarTurn + 0), 1);
     mbar_init(c.bar(kBarTurn + 1), 1);
     *c.abort_flag = 0u;
+    reinterpret_cast<volatile int*>(smem + kOffFail)[0] = 0;
+    reinterpret_cast<volatile int*>(smem + kOffFail)[1] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -260,9 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = kv_smem + s * kTileBytes;
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         const int row = (t >> 1) * kBlock;
-        mbar_arrive_expect_tx(bar, kTileBytes);
-        tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, keep);
-        tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
+        if (t != p.withhold) {
+          mbar_arrive_expect_tx(bar, kTileBytes);
+          tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, keep);
+          tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
+        }
         issued = t + 1;
         if (t == 0) load_q(1);
         if (++s == kStages) s = 0;
@@ -271,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
         for (int q = 0; q < 2; ++q) wait_slow(c, kBarQFull + q, 0, kRoleLoad, false, kDrainLimitNs);
         for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
-          wait_slow(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleLoad, false, kDrainLimitNs);
+          if (t != p.withhold)
+            wait_slow(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleLoad, false, kDrainLimitNs);
       }
     }
     __syncwarp();
@@ -281,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp >> 2;
     const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
     const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
+    volatile int* const fail_sm = reinterpret_cast<volatile int*>(smem + kOffFail);
     const float sl2 = p.scale_log2;
     const int rem = p.S - (p.n_kv - 1) * kBlock;  // valid keys in the last tile, 1..128
     float m_kept = -INFINITY;                 // kept row max, base-2 units
@@ -370,12 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(c.bar(kBarTurn + (q ^ 1)));  // G_q(0) issued
       }
     }
-    __syncwarp();
+    // The warp-collective waits below need one value of ok in the whole warp.
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 
-    for (int i = 0; i < n && ok; ++i) {
+    for (int i = 0; i < n; ++i) {
       // S_q(i) full also means every earlier MMA of this Q tile, so PV_q(i-1) has read
-      // P_q(i-1).
-      if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) { ok = false; break; }
+      // P_q(i-1). A warp whose leader gave up in the previous iteration waits no more.
+      if (!(ok && wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax))) {
+        // Give up: record the iteration for the other three warps, release them from this
+        // iteration's barrier and leave. They read the record after the barrier and leave at
+        // the same iteration, so no warp is ever left waiting there.
+        fail_sm[q] = i + 1;
+        named_bar_sync(2 + q, 128);
+        ok = false;
+        break;
+      }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld32_x128_sync(tS, sr);
@@ -450,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32_x64(tS, pk);
       tmem_wait_st();
       tc_fence_before();
-      named_bar_sync(2 + q, 128);  // P_q(i) stored by all four warps
+      named_bar_sync(2 + q, 128);  // P_q(i) stored by all four warps (or one gave up)
       if (leader) {
         tc_fence_after();
         const int tv = 2 * i + 1, tk = 2 * i + 2;
@@ -485,8 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      // A record of i + 1 or less was written before this iteration's barrier by a warp that
+      // gave up; a later one (a warp already in the next iteration) is read again next time.
+      const int f = fail_sm[q];
+      if (f != 0 && f <= i + 1) { ok = false; break; }
     }
-    if (leader && !ok) {
+    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the leader
+    // issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
+    const bool fin = ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax);
+    if (leader && !fin) {
       // Give up: make sure every MMA this thread issued has finished before TMEM is freed.
       mma_commit(c.bar(kBarMmaDone + q));
       wait_slow(c, kBarMmaDone + q, 0, kRoleSoftmax, false, kDrainLimitNs);
@@ -494,9 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     // epilogue: O / l -> BF16 -> SW128 staging in the dead Q_q buffer -> one TMA store of
     // this warp's 32 rows (no cross-warp barrier; the two Q tiles finish independently).
-    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the leader
-    // issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
-    if (ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax)) {
+    if (fin) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256u + q * 128u;
@@ -697,7 +723,7 @@ extern "C" {
 static int attn_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                        int S, int D, float scale, const long long* qs, const long long* ks,
                        const long long* vs, const long long* os, int rebase_threshold_log2,
-                       int causal, void* stream) {
+                       int causal, int withhold, void* stream) {
   using namespace gb300;
   if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
@@ -708,6 +734,8 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qp = (static_cast<long long>(S) + 2 * kBlock - 1) / (2 * kBlock);
   if (BH > (1ll << 31) - 1 || BH * n_qp > (1ll << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  const long long n_kv = (static_cast<long long>(S) + kBlock - 1) / kBlock;
+  if (withhold < -1 || withhold >= 2 * n_kv) return ATTN_ERR_INVALID_ARG;
   long long st[4][3];
   const long long* in[4] = {qs, ks, vs, os};
   for (int t = 0; t < 4; ++t) {
@@ -745,10 +773,11 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   prm.lse = lse;
   prm.S = S;
   prm.H = H;
-  prm.n_kv = static_cast<int>((S + kBlock - 1) / kBlock);
+  prm.n_kv = static_cast<int>(n_kv);
   prm.n_qp = static_cast<int>(n_qp);
   prm.BH = static_cast<int>(BH);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.withhold = withhold;
 
   const dim3 grid(static_cast<unsigned>(BH * n_qp));
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
@@ -767,7 +796,8 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 int S, int D, float scale, int rebase_threshold_log2, void* stream) {
   // Contiguous [B, H, S, D]: element strides (H*S*D, S*D, D).
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, 0, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, 0, -1,
+                     stream);
 }
 
 int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -775,13 +805,20 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
                      const long long* v_strides, const long long* o_strides, int rebase_threshold_log2,
                      int causal, void* stream) {
   return attn_launch(q, k, v, o, lse, B, H, S, D, scale, q_strides, k_strides, v_strides, o_strides,
-                     rebase_threshold_log2, causal, stream);
+                     rebase_threshold_log2, causal, -1, stream);
 }
 
 int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                     int S, int D, float scale, void* stream) {
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, -1, stream);
+}
+
+int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int S, int D, float scale, int token, void* stream) {
+  if (token < 0) return ATTN_ERR_INVALID_ARG;
+  const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 0, token, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

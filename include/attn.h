@@ -126,8 +126,25 @@ const char* attn_status_string(int status);
  * non-zero word here (the first failure wins). Call it after synchronising the streams that
  * ran attn_fwd. *word receives 0 when no wait gave up. Returns ATTN_OK, or
  * ATTN_ERR_UNSUPPORTED_DEVICE / ATTN_ERR_LAUNCH if the word could not be read.
+ *
+ * Word layout: 0xA77E0000 | role << 8 | barrier, role 1 = TMA producer, 3 = softmax / MMA
+ * issue, 4 = O correction; barrier = the index of the mbarrier whose wait ran out.
  */
 int attn_device_status(unsigned int* word, int reset);
+
+/*
+ * attn_fwd_withhold -- test hook for the bounded waits. Runs attn_fwd (dense, rebase
+ * threshold 0) except that every CTA's TMA producer skips K/V token `token` (token 2i is
+ * K tile i, token 2i+1 is V tile i, tiles of 128 keys), so the waits that need it never
+ * complete. About two seconds after launch the first such wait gives up and records its
+ * status word (see attn_device_status); every CTA then drains its own loads and MMAs, frees
+ * its tensor memory and exits, and the context stays usable. O and lse are left undefined.
+ *
+ *   token : 0 <= token < 2 * ceil(S / 128), else ATTN_ERR_INVALID_ARG.
+ * Other arguments, errors and ownership as attn_fwd. Nothing a user needs calls this.
+ */
+int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int S, int D, float scale, int token, void* stream);
 
 /* Library version, (major << 16) | minor. */
 int attn_version(void);

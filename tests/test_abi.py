@@ -31,7 +31,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_causal", "attn_fwd_ex",
-                                  "attn_fwd_strided", "attn_status_string", "attn_version"]
+                                  "attn_fwd_strided", "attn_fwd_withhold", "attn_status_string",
+                                  "attn_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -115,6 +116,18 @@ def test_causal_argument_errors(lib, kw, expected):
     a.update(kw)
     assert lib.attn_fwd_causal(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["S"], a["D"],
                                a["scale"], None) == expected
+
+
+@pytest.mark.parametrize("S,token,expected", [
+    (256, -1, 1), (256, -5, 1), (256, 4, 1), (300, 6, 1), (256, 3, 4), (300, 5, 4),
+])
+def test_withhold_token_range(lib, S, token, expected):
+    """The test hook accepts only a token the CTAs walk (2 per 128-key tile); a valid call
+    reaches the device check, which fails here without a GPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.attn_fwd_withhold(Q, K, V, O, L, 1, 1, S, 128, 0.088, token, None) == expected
 
 
 def test_no_device_is_reported(lib):
