@@ -8,9 +8,11 @@ from __future__ import annotations
 
 import math
 
-from ._lib import AttnError, attn_fwd, attn_fwd_ex, attn_fwd_strided, device_status, lib  # noqa: F401
+from ._lib import (AttnError, attn_fwd, attn_fwd_ex, attn_fwd_strided, check_device_status,  # noqa: F401
+                   device_status, lib)
 
-__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "AttnError", "lib"]
+__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "check_device_status",
+           "AttnError", "lib"]
 
 
 def _check(name, t, shape=None):

@@ -115,3 +115,15 @@ def device_status(reset: bool = True) -> int:
     if st != ATTN_OK:
         raise AttnError(st, "attn_device_status")
     return word.value
+
+
+_ROLES = {1: "TMA producer", 2: "MMA issue", 3: "softmax / MMA issue", 4: "O correction"}
+
+
+def check_device_status(reset: bool = True) -> None:
+    """Raise AttnError(ATTN_ERR_TIMEOUT) if a kernel gave up a bounded wait since the word was
+    last cleared (call after synchronising the streams that ran the kernels)."""
+    word = device_status(reset)
+    if word != 0:
+        role = _ROLES.get((word >> 8) & 0xFF, "unknown role")
+        raise AttnError(6, f"kernel (status word {word:#010x}: {role}, mbarrier {word & 0xFF})")

@@ -30,7 +30,8 @@ typedef enum {
     ATTN_ERR_MISALIGNED = 3,         /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned */
     ATTN_ERR_UNSUPPORTED_DEVICE = 4, /* no CUDA device, or the current device is not sm_103 */
     ATTN_ERR_LAUNCH = 5,             /* tensor-map encoding or kernel launch failed */
-    ATTN_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait (see attn_device_status) */
+    ATTN_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait: attn_device_status returns the
+                                        word; the Python binding's check_device_status raises this code */
 } attn_status;
 
 /*

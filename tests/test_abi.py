@@ -141,6 +141,15 @@ def test_no_device_is_reported(lib):
     assert lib.attn_device_status(None, 0) == 1
 
 
+def test_status_check_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(attn.AttnError) as e:
+        attn.check_device_status()
+    assert e.value.status == 4  # the word cannot be read: ATTN_ERR_UNSUPPORTED_DEVICE
+
+
 def test_python_wrapper_rejects_cpu_and_wrong_dtype():
     import torch
     x = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)

@@ -40,10 +40,14 @@ def test_withheld_token_gives_up_cleanly(token):
     assert st == 0
     torch.cuda.synchronize()
     elapsed = time.monotonic() - t0
-    word = attn.device_status(reset=True)
+    word = attn.device_status(reset=False)
     assert word >> 16 == 0xA77E, hex(word)
     assert (word >> 8) & 0xFF in ROLES, hex(word)
     assert (word & 0xFF) < 16, hex(word)
+    with pytest.raises(attn.AttnError) as e:
+        attn.check_device_status(reset=True)
+    assert e.value.status == 6  # ATTN_ERR_TIMEOUT
+    attn.check_device_status()  # cleared
     assert 1.5 < elapsed < 30.0, elapsed
     # The context is intact: an ordinary call on the same inputs matches the oracle and no
     # wait gives up.
