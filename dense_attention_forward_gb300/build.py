@@ -4,6 +4,9 @@ Produces, next to this file:
   libattn.so          -- the product: attn_fwd and friends, the C ABI of include/attn.h
   libattn_selftest.so -- single-tile tcgen05 GEMM checks used by the GPU tests
 
+build_trace() makes libattn_trace.so on demand (the same kernels with -DATTN_TRACE, see
+include/attn_trace.h); the ordinary build does not.
+
 Both are plain shared libraries (static CUDA runtime; the driver is loaded lazily at the
 first CUDA call), so they load on a machine without a GPU.
 """
@@ -37,14 +40,14 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set NVCC or put /usr/local/cuda/bin on PATH)")
 
 
-def _compile(target: str, sources: list[str], verbose: bool) -> str:
+def _compile(target: str, sources: list[str], verbose: bool, defines: tuple = ()) -> str:
     out = os.path.join(PKG, target)
     srcs = [os.path.join(CSRC, s) for s in sources]
     deps = srcs + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "attn.h")]
     if os.path.exists(out) and all(os.path.getmtime(out) >= os.path.getmtime(d) for d in deps):
         return out
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, *FLAGS, "-Xptxas", "-v", "-o", tmp, *srcs]
+    cmd = [nvcc(), *ARCH, *FLAGS, *defines, "-Xptxas", "-v", "-o", tmp, *srcs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if verbose or res.returncode != 0:
         sys.stderr.write(res.stdout + res.stderr)
@@ -58,6 +61,11 @@ def build(verbose: bool = False) -> list[str]:
     with ThreadPoolExecutor(max_workers=len(TARGETS)) as ex:
         futs = [ex.submit(_compile, t, s, verbose) for t, s in TARGETS.items()]
         return [f.result() for f in futs]
+
+
+def build_trace(verbose: bool = False) -> str:
+    """libattn_trace.so: libattn.so's kernels with the timeline stamps compiled in."""
+    return _compile("libattn_trace.so", ["attn_fwd.cu"], verbose, ("-DATTN_TRACE",))
 
 
 if __name__ == "__main__":

@@ -94,6 +94,37 @@ enum : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleCorrection
 
 __device__ unsigned int g_attn_status = 0;
 
+// Optional timeline trace (built only into libattn_trace.so, with -DATTN_TRACE): per CTA, the
+// globaltimer at entry (0), after setup (1), when Q tile 0's first S is seen (2), when O_0 and
+// O_1 are full (3, 4), before the final barrier (5), the SM id (6) and at exit (7). In the
+// ordinary build the stamps compile to nothing.
+#ifdef ATTN_TRACE
+#ifndef ATTN_TRACE_CTAS
+#define ATTN_TRACE_CTAS 4096
+#endif
+__device__ unsigned long long g_attn_trace[ATTN_TRACE_CTAS * 8];
+__device__ __forceinline__ unsigned sm_id() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+#define ATTN_STAMP(k)                                                                        \
+  do {                                                                                       \
+    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * 8u + (k)] = global_timer_ns(); \
+  } while (0)
+#define ATTN_STAMP_SM()                                                   \
+  do {                                                                    \
+    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * 8u + 6] = sm_id(); \
+  } while (0)
+#else
+#define ATTN_STAMP(k) \
+  do {                \
+  } while (0)
+#define ATTN_STAMP_SM() \
+  do {                  \
+  } while (0)
+#endif
+
 struct Params {
   float* lse;
   int S;            // sequence length
@@ -188,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qp * 2 * kBlock;
   const int n = kCausal ? min(p.n_kv, 2 * qp + 2) : p.n_kv;  // K/V tiles this CTA walks
 
+  if (threadIdx.x == 0) {
+    ATTN_STAMP(0);
+    ATTN_STAMP_SM();
+  }
   Ctl c;
   c.bar0 = base + kOffBar;
   c.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
@@ -224,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) ATTN_STAMP(1);
 
   // Register split (warpgroup granularity, set at the top of each role's branch so the
   // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 64 +
@@ -397,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      if (i == 0 && warp == 0 && lane == 0) ATTN_STAMP(2);
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld32_x128_sync(tS, sr);
@@ -514,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the leader
     // issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
     const bool fin = ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax);
+    if ((warp & 3) == 0 && lane == 0) ATTN_STAMP(3 + q);
     if (leader && !fin) {
       // Give up: make sure every MMA this thread issued has finished before TMEM is freed.
       mma_commit(c.bar(kBarMmaDone + q));
@@ -593,12 +631,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (threadIdx.x == 0) ATTN_STAMP(5);
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) ATTN_STAMP(7);
 }
 
 }  // namespace gb300
@@ -863,5 +903,27 @@ int attn_device_status(unsigned int* word, int reset) {
 }
 
 int attn_version(void) { return (1 << 16) | 0; }
+
+#ifdef ATTN_TRACE
+int attn_trace_read(unsigned long long* out, int max_ctas) {
+  if (!out || max_ctas <= 0) return ATTN_ERR_INVALID_ARG;
+  const int nct = max_ctas < ATTN_TRACE_CTAS ? max_ctas : ATTN_TRACE_CTAS;
+  if (cudaMemcpyFromSymbol(out, gb300::g_attn_trace, static_cast<size_t>(nct) * 8 * sizeof(unsigned long long)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+int attn_trace_clear(void) {
+  static unsigned long long zero[ATTN_TRACE_CTAS * 8];
+  if (cudaMemcpyToSymbol(gb300::g_attn_trace, zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+#endif
 
 }  // extern "C"
