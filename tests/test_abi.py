@@ -41,6 +41,20 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_symbols()) == set(_lib.SIGNATURES)
 
 
+def test_trace_build_exports_both_headers(lib):
+    """libattn_trace.so (built on demand) exports attn.h and attn_trace.h; libattn.so does not
+    export the trace entry points."""
+    from dense_attention_forward_gb300 import build
+    trace_header = os.path.join(ROOT, "include", "attn_trace.h")
+    trace_syms = sorted(set(re.findall(r"^\s*int\s+(attn_\w+)\s*\(", open(trace_header).read(), re.M)))
+    assert trace_syms == ["attn_trace_clear", "attn_trace_read"]
+    tl = ctypes.CDLL(build.build_trace())
+    for name in declared_symbols() + trace_syms:
+        assert hasattr(tl, name), name
+    for name in trace_syms:
+        assert not hasattr(lib, name), name
+
+
 def test_version_and_status_strings(lib):
     assert lib.attn_version() >> 16 == 1
     for code in range(7):
