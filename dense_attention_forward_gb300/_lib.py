@@ -82,6 +82,8 @@ def selftest_lib():
         h.attn_selftest_gemm.restype = ctypes.c_int
         h.attn_selftest_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int, ctypes.c_void_p]
+        h.attn_selftest_elementwise.restype = ctypes.c_int
+        h.attn_selftest_elementwise.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p]
         _selftest = h
     return _selftest
 

@@ -5,6 +5,8 @@
 //   mode 2: C = A B,   A packed BF16 in tensor memory, B MN-major     (the O += P V form)
 // A is [128 x 128] row-major BF16 (M x K); B is [128 N x 128 K] (mode 0) or [128 K x 128 N]
 // (modes 1, 2) row-major BF16; C is [128 x 128] row-major fp32. One CTA of 128 threads.
+// attn_selftest_elementwise runs the softmax's per-element helpers (MUFU exp2, BF16 packing
+// and unpacking, three-input max) on arrays, for comparison with exact host values.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -139,8 +141,34 @@ bool encode_tile(CUtensorMap* m, const void* p) {
                       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per element i: f[4i] = 2^x[i] (MUFU, ftz), u[i] = BF16x2 of (x[i], y[i]) (round to
+// nearest even, x in the low half), f[4i+1], f[4i+2] = that pair widened back to fp32,
+// f[4i+3] = max(x[i], y[i], -x[i]).
+__global__ void selftest_elementwise_kernel(const float* __restrict__ x, const float* __restrict__ y,
+                                           uint32_t* __restrict__ u, float* __restrict__ f, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const uint32_t pk = pack_bf16x2(x[i], y[i]);
+    float lo, hi;
+    bf16x2_to_f32x2(pk, lo, hi);
+    u[i] = pk;
+    f[4 * i + 0] = ex2_ftz(x[i]);
+    f[4 * i + 1] = lo;
+    f[4 * i + 2] = hi;
+    f[4 * i + 3] = max3(x[i], y[i], -x[i]);
+  }
+}
+
 }  // namespace
 }  // namespace gb300
+
+extern "C" int attn_selftest_elementwise(const float* x, const float* y, unsigned int* u, float* f, int n,
+                                         void* stream) {
+  using namespace gb300;
+  if (!x || !y || !u || !f || n <= 0) return 1;
+  selftest_elementwise_kernel<<<(n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024, 256, 0,
+                                static_cast<cudaStream_t>(stream)>>>(x, y, u, f, n);
+  return cudaGetLastError() == cudaSuccess ? 0 : 5;
+}
 
 extern "C" int attn_selftest_gemm(const void* a, const void* b, float* c, int mode, void* stream) {
   using namespace gb300;
