@@ -70,6 +70,13 @@ def timeline(B: int, H: int, S: int, causal: bool = False, seed: int = 0) -> dic
     if lib.attn_trace_read(buf, cap) != 0:
         raise RuntimeError("attn_trace_read failed")
     t = np.frombuffer(buf, dtype=np.uint64).reshape(cap, 8).astype(np.int64)
+    return summarize(t, n, f"B={B} H={H} S={S} D=128" + (" causal" if causal else ""))
+
+
+def summarize(t: np.ndarray, n: int, workload: str) -> dict:
+    """Phase means (microseconds) of a [ctas, 8] array of trace words (layout in
+    include/attn_trace.h); n is the launch's CTA count."""
+    cap = t.shape[0]
     ends = np.maximum(t[:, 3], t[:, 4])
     gaps = []
     for sm in np.unique(t[:, 6]):
@@ -81,7 +88,7 @@ def timeline(B: int, H: int, S: int, causal: bool = False, seed: int = 0) -> dic
         return round(float(np.mean(a)) / 1e3, 3)
 
     return {
-        "workload": f"B={B} H={H} S={S} D=128" + (" causal" if causal else ""),
+        "workload": workload,
         "ctas": n, "ctas_traced": cap, "sms": int(len(np.unique(t[:, 6]))),
         "span_us": round(float(t[:, 7].max() - t[:, 0].min()) / 1e3, 1),
         "cta_us": mean_us(t[:, 7] - t[:, 0]),
