@@ -34,7 +34,7 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
 # valid only for the kernel source it was taken on (hash of the CUDA sources).
-TRAFFIC = {"s4k": (247037696, "f8a0515accc877ba")}  # ncu: 201,382,912 B read + 45,654,784 B written
+TRAFFIC = {"s4k": (246194944, "ecaf6eb2a7824564")}  # ncu: 201,383,680 B read + 44,811,264 B written
 
 
 def source_hash() -> str:
@@ -239,41 +239,20 @@ def run_gpu(args, w):
     value = job_throughput(w.flops, kern_ms, world)
     status = attn.device_status(reset=True)
 
-    # ---- end to end: pinned host -> device, attn_fwd, device -> pinned host, every step.
-    # Steps are pipelined the way a serving loop would run them: two device buffer sets,
-    # the copy-in of step k on one stream, the kernel on another, the copy-out on a third,
-    # so step k's copy-in overlaps step k-1's kernel and step k-2's copy-out. Every step
-    # still moves all of its inputs in and its outputs out.
+    # ---- end to end: the library's host-to-host call (attn_fwd_host) every step: pinned host
+    # q, k, v -> device, the kernel, device -> pinned host o and lse. Steps alternate between
+    # two streams, each with its own device and output buffers, so step k+1's copy-in overlaps
+    # step k's kernel and copy-out, as a serving loop would run them. Every step still moves
+    # all of its inputs in and its outputs out.
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
     oh = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     lh = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     bufs = [tuple(torch.empty_like(t) for t in (q, k, v, o)) + (torch.empty_like(lse),) for _ in range(2)]
-    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    for b in range(2):  # buffers start free
-        ev_cmp[b].record(s_cmp)
-        ev_out[b].record(s_out)
+    streams = [torch.cuda.Stream(dev) for _ in range(2)]
 
     def e2e_step(kstep):
         b = kstep & 1
-        qd, kd, vd, od, ld = bufs[b]
-        s_in.wait_event(ev_cmp[b])          # step k-2's kernel no longer reads these inputs
-        with torch.cuda.stream(s_in):
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-        ev_in[b].record(s_in)
-        s_cmp.wait_event(ev_in[b])
-        s_cmp.wait_event(ev_out[b])         # step k-2's outputs have left the device
-        attn.fwd(qd, kd, vd, w.scale, out=od, lse=ld, stream=s_cmp)
-        ev_cmp[b].record(s_cmp)
-        s_out.wait_event(ev_cmp[b])
-        with torch.cuda.stream(s_out):
-            oh[b].copy_(od, non_blocking=True)
-            lh[b].copy_(ld, non_blocking=True)
-        ev_out[b].record(s_out)
+        attn.fwd_host(qh, kh, vh, w.scale, out=oh[b], lse=lh[b], dev=bufs[b], stream=streams[b])
 
     for kstep in range(4):
         e2e_step(kstep)
@@ -281,11 +260,11 @@ def run_gpu(args, w):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e0.record(stream)
-    for st_ in (s_in, s_cmp, s_out):
+    for st_ in streams:
         st_.wait_stream(stream)
     for kstep in range(e2e_steps):
         e2e_step(kstep)
-    for st_ in (s_in, s_cmp, s_out):
+    for st_ in streams:
         stream.wait_stream(st_)
     e1.record(stream)
     barrier()
@@ -349,7 +328,7 @@ def run_gpu(args, w):
                      "peak_source": f"{peaks_src} bf16_tflops (burst, cuBLAS 8192^3)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "schedule": "pipelined: 2 device buffer sets; copy-in, kernel, copy-out on 3 streams"},
+                "schedule": "attn_fwd_host per step (copy-in, kernel, copy-out), steps alternating over 2 streams with their own buffers"},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 3),

@@ -11,7 +11,7 @@ import math
 from ._lib import (AttnError, attn_fwd, attn_fwd_ex, attn_fwd_strided, check_device_status,  # noqa: F401
                    device_status, lib)
 
-__all__ = ["fwd", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "check_device_status",
+__all__ = ["fwd", "fwd_host", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "check_device_status",
            "AttnError", "lib"]
 
 
@@ -78,3 +78,43 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     if st != 0:
         raise AttnError(st)
     return out, lse
+
+
+def fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, dev=None, causal: bool = False,
+             stream=None):
+    """attn_fwd_host: host q, k, v in, host o and lse out, through the caller's device buffers.
+
+    q, k, v: contiguous CPU bfloat16 tensors [B, H, S, 128] (pinned for asynchronous copies);
+    scale defaults to 1/sqrt(128).
+    out, lse: CPU tensors to receive o (bfloat16) and lse (float32); pinned ones are created if
+    not given. dev: (q_d, k_d, v_d, o_d, lse_d) CUDA tensors of the same shapes, created on the
+    current device if not given. The call only enqueues work on `stream` (default: the current
+    stream): synchronise before reading out / lse. Returns (out, lse, dev).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU bfloat16 tensor")
+        if t.dim() != 4 or tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must be [B, H, S, D] like q")
+    B, H, S, D = q.shape
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    for name, t, dt, shape in (("out", out, torch.bfloat16, (B, H, S, D)), ("lse", lse, torch.float32, (B, H, S))):
+        if t.is_cuda or t.dtype != dt or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of shape {shape}")
+    if dev is None:
+        dev = tuple(torch.empty((B, H, S, D), device="cuda", dtype=torch.bfloat16) for _ in range(4)) + (
+            torch.empty((B, H, S), device="cuda", dtype=torch.float32),)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev[0].device)
+    with torch.cuda.device(dev[0].device):
+        st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 *(t.data_ptr() for t in dev), B, H, S, D,
+                                 float(scale if scale is not None else 1.0 / math.sqrt(D)),
+                                 int(bool(causal)), stream.cuda_stream)
+    if st != 0:
+        raise AttnError(st, "attn_fwd_host")
+    return out, lse, dev

@@ -763,7 +763,7 @@ extern "C" {
 static int attn_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                        int S, int D, float scale, const long long* qs, const long long* ks,
                        const long long* vs, const long long* os, int rebase_threshold_log2,
-                       int causal, int withhold, void* stream) {
+                       int causal, int withhold, int check_only, void* stream) {
   using namespace gb300;
   if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
@@ -803,6 +803,7 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   const int status = prepare_device(&dev);
   if (status != ATTN_OK) return status;
   if (!get_encoder()) return ATTN_ERR_LAUNCH;
+  if (check_only) return ATTN_OK;
 
   CUtensorMap tq, tk, tv, to;
   if (!encode_4d(&tq, q, B, H, S, st[0]) || !encode_4d(&tk, k, B, H, S, st[1]) ||
@@ -836,7 +837,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 int S, int D, float scale, int rebase_threshold_log2, void* stream) {
   // Contiguous [B, H, S, D]: element strides (H*S*D, S*D, D).
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, 0, -1,
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, rebase_threshold_log2, 0, -1, 0,
                      stream);
 }
 
@@ -845,20 +846,48 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
                      const long long* v_strides, const long long* o_strides, int rebase_threshold_log2,
                      int causal, void* stream) {
   return attn_launch(q, k, v, o, lse, B, H, S, D, scale, q_strides, k_strides, v_strides, o_strides,
-                     rebase_threshold_log2, causal, -1, stream);
+                     rebase_threshold_log2, causal, -1, 0, stream);
 }
 
 int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                     int S, int D, float scale, void* stream) {
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, -1, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, -1, 0, stream);
 }
 
 int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                       int S, int D, float scale, int token, void* stream) {
   if (token < 0) return ATTN_ERR_INVALID_ARG;
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 0, token, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 0, token, 0, stream);
+}
+
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d,
+                  void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int S, int D, float scale,
+                  int causal, void* stream) {
+  if (!q_h || !k_h || !v_h || !o_h) return ATTN_ERR_INVALID_ARG;
+  if ((lse_h == nullptr) != (lse_d == nullptr)) return ATTN_ERR_INVALID_ARG;
+  const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
+  // Everything the kernel launch would reject is rejected before any copy is enqueued.
+  int r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 1, stream);
+  if (r != ATTN_OK) return r;
+  const size_t bytes = static_cast<size_t>(B) * H * S * D * 2;
+  const size_t lse_bytes = static_cast<size_t>(B) * H * S * 4;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(q_d, q_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(k_d, k_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(v_d, v_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 0, stream);
+  if (r != ATTN_OK) return r;
+  if (cudaMemcpyAsync(o_h, o_d, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (lse_h && cudaMemcpyAsync(lse_h, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

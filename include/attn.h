@@ -116,6 +116,29 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
                      const long long* v_strides, const long long* o_strides,
                      int rebase_threshold_log2, int causal, void* stream);
 
+/*
+ * attn_fwd_host -- attn_fwd (or attn_fwd_causal) from HOST buffers to HOST buffers: enqueues on
+ * `stream` the copies of q_h, k_h, v_h into the caller's device buffers q_d, k_d, v_d, the
+ * kernel, and the copies of o_d and lse_d back into o_h and lse_h, then returns. Synchronise
+ * the stream before reading o_h / lse_h or reusing any of the buffers.
+ *
+ *   q_h, k_h, v_h : HOST pointers, BF16, contiguous [B, H, S, D]; read by the copies.
+ *   o_h           : HOST pointer, BF16 [B, H, S, D], written by the copy-out.
+ *   lse_h         : HOST pointer, fp32 [B, H, S], or NULL (then lse_d must be NULL too).
+ *   q_d .. lse_d  : DEVICE buffers of the same shapes, owned by the caller, with attn_fwd's
+ *                   alignment and no-overlap rules; the library allocates nothing.
+ *   causal        : 0 = attn_fwd, 1 = attn_fwd_causal.
+ * Host buffers should be page-locked (cudaHostAlloc, or a pinned torch tensor) for the copies
+ * to run asynchronously and overlap other streams; pageable memory still works, with the
+ * CUDA runtime's staging.
+ * Errors: every check attn_fwd makes is made before anything is enqueued, plus NULL host
+ * pointers and an lse_h / lse_d mismatch (ATTN_ERR_INVALID_ARG); a failed copy is
+ * ATTN_ERR_LAUNCH.
+ */
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                  void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                  int B, int H, int S, int D, float scale, int causal, void* stream);
+
 /* A short, static, human-readable description of a status code. Never NULL. */
 const char* attn_status_string(int status);
 

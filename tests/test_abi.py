@@ -31,8 +31,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_causal", "attn_fwd_ex",
-                                  "attn_fwd_strided", "attn_fwd_withhold", "attn_status_string",
-                                  "attn_version"]
+                                  "attn_fwd_host", "attn_fwd_strided", "attn_fwd_withhold",
+                                  "attn_status_string", "attn_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -142,6 +142,32 @@ def test_withhold_token_range(lib, S, token, expected):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.attn_fwd_withhold(Q, K, V, O, L, 1, 1, S, 128, 0.088, token, None) == expected
+
+
+# Fake host addresses (never dereferenced: every case fails before a copy is enqueued).
+QH, KH, VH, OH, LH = 0x61000000, 0x62000000, 0x63000000, 0x64000000, 0x65000000
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q_h=None), 1), (dict(k_h=None), 1), (dict(v_h=None), 1), (dict(o_h=None), 1),
+    (dict(lse_h=None), 1), (dict(lse_d=None), 1), (dict(D=64), 2), (dict(S=0), 1), (dict(causal=2), 1),
+    (dict(o_d=Q), 1), (dict(q_d=Q + 8), 3),
+])
+def test_host_entry_argument_errors(lib, kw, expected):
+    a = dict(q_h=QH, k_h=KH, v_h=VH, o_h=OH, lse_h=LH, q_d=Q, k_d=K, v_d=V, o_d=O, lse_d=L,
+             B=1, H=1, S=256, D=128, scale=0.088, causal=0)
+    a.update(kw)
+    assert lib.attn_fwd_host(a["q_h"], a["k_h"], a["v_h"], a["o_h"], a["lse_h"], a["q_d"], a["k_d"], a["v_d"],
+                             a["o_d"], a["lse_d"], a["B"], a["H"], a["S"], a["D"], a["scale"], a["causal"],
+                             None) == expected
+
+
+def test_host_entry_without_lse_and_without_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # Valid arguments reach the device check (nothing is enqueued without a GPU).
+    assert lib.attn_fwd_host(QH, KH, VH, OH, None, Q, K, V, O, None, 1, 1, 256, 128, 0.088, 0, None) == 4
 
 
 def test_no_device_is_reported(lib):
