@@ -90,6 +90,42 @@ def test_probability_rows_sum_to_one_and_are_positive():
     assert np.allclose(p.sum(axis=-1), 1.0, atol=1e-14)
 
 
+def test_probabilities_two_keys_with_a_non_unit_scale():
+    # Raw scores 2 ln 3 and 0 at scale 1/2 are ln 3 and 0: weights exactly 3/4 and 1/4. A
+    # dropped scale gives 9/10 and 1/10, a doubled one 81/82 and 1/82.
+    q = np.array([[[1.0], [-1.0]]])
+    k = np.array([[[2.0 * math.log(3.0)], [0.0]]])
+    p = ref.probabilities(q, k, 0.5)
+    assert np.allclose(p[0, 0], [0.75, 0.25], atol=1e-15)
+    assert np.allclose(p[0, 1], [0.25, 0.75], atol=1e-15)  # row 1: scores -ln 3 and 0
+
+
+def test_probabilities_times_values_is_the_attention_output():
+    # softmax(scale Q K^T) V is O by the definition; attention() is pinned independently
+    # (brute force, closed forms, torch SDPA), so a wrong scale, axis or transpose in
+    # probabilities() shows here.
+    q, k, v = _rand(3, 23, 6, gain=2.0), _rand(3, 23, 6, gain=2.0), _rand(3, 23, 4)
+    p = ref.probabilities(q, k, 0.37)
+    o, _ = ref.attention(q, k, v, 0.37)
+    assert p.shape == (3, 23, 23)
+    assert np.max(np.abs(p @ v - o)) < 1e-13
+
+
+def test_probabilities_match_bruteforce_on_large_scores():
+    # Entries written out with math.exp around each row's own maximum; scores of order 10^3
+    # overflow unless the maximum is taken along the key axis of each row.
+    q, k = _rand(1, 7, 3, gain=25.0), _rand(1, 7, 3, gain=25.0)
+    scale = 0.8
+    p = ref.probabilities(q, k, scale)
+    for i in range(7):
+        s = [scale * sum(q[0, i, d] * k[0, j, d] for d in range(3)) for j in range(7)]
+        mx = max(s)
+        e = [math.exp(x - mx) for x in s]
+        tot = sum(e)
+        for j in range(7):
+            assert abs(p[0, i, j] - e[j] / tot) < 1e-13
+
+
 def test_output_is_convex_combination_of_values():
     q, k, v = _rand(1, 64, 8, gain=2.0), _rand(1, 64, 8, gain=2.0), _rand(1, 64, 8)
     o, _ = ref.attention(q, k, v, 0.5)
