@@ -80,6 +80,24 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     return out, lse
 
 
+def _check_device_buffers(dev, B, H, S, D):
+    """fwd_host's `dev`: (q_d, k_d, v_d, o_d, lse_d), contiguous bfloat16 [B, H, S, D] x 4 and
+    float32 [B, H, S], all CUDA tensors on one device (the C call writes into them by address,
+    so a smaller buffer would be overrun)."""
+    import torch
+    if not isinstance(dev, (tuple, list)) or len(dev) != 5:
+        raise ValueError("dev must be a tuple (q_d, k_d, v_d, o_d, lse_d)")
+    names = ("q_d", "k_d", "v_d", "o_d", "lse_d")
+    for i, (name, t) in enumerate(zip(names, dev)):
+        dt, shape = (torch.float32, (B, H, S)) if i == 4 else (torch.bfloat16, (B, H, S, D))
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != dev[0].device:
+            raise ValueError("the device buffers must all be on one device")
+
+
 def fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, dev=None, causal: bool = False,
              stream=None):
     """attn_fwd_host: host q, k, v in, host o and lse out, through the caller's device buffers.
@@ -87,8 +105,9 @@ def fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, dev=None, 
     q, k, v: contiguous CPU bfloat16 tensors [B, H, S, 128] (pinned for asynchronous copies);
     scale defaults to 1/sqrt(128).
     out, lse: CPU tensors to receive o (bfloat16) and lse (float32); pinned ones are created if
-    not given. dev: (q_d, k_d, v_d, o_d, lse_d) CUDA tensors of the same shapes, created on the
-    current device if not given. The call only enqueues work on `stream` (default: the current
+    not given. dev: (q_d, k_d, v_d, o_d, lse_d) contiguous CUDA tensors of the same shapes on one
+    device (checked: shape, dtype, contiguity, device), created on the current device if not
+    given; `stream`, when given, must be on that device. The call only enqueues work on `stream` (default: the current
     stream): synchronise before reading out / lse. Returns (out, lse, dev).
     """
     import torch
@@ -108,8 +127,12 @@ def fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, dev=None, 
     if dev is None:
         dev = tuple(torch.empty((B, H, S, D), device="cuda", dtype=torch.bfloat16) for _ in range(4)) + (
             torch.empty((B, H, S), device="cuda", dtype=torch.float32),)
+    else:
+        _check_device_buffers(dev, B, H, S, D)
     if stream is None:
         stream = torch.cuda.current_stream(dev[0].device)
+    elif stream.device != dev[0].device:
+        raise ValueError(f"stream is on {stream.device}, the device buffers on {dev[0].device}")
     with torch.cuda.device(dev[0].device):
         st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                  *(t.data_ptr() for t in dev), B, H, S, D,

@@ -7,6 +7,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libattn.so")
 SELFTEST_PATH = os.path.join(PKG, "libattn_selftest.so")
+TEST_HOOKS_PATH = os.path.join(PKG, "libattn_testhooks.so")
 
 ATTN_OK = 0
 STATUS_NAMES = {
@@ -36,10 +37,6 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                        ctypes.c_void_p]),
-    "attn_fwd_withhold": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
-                                         ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_int] * 4 +
                       [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -47,8 +44,17 @@ SIGNATURES = {
     "attn_version": (ctypes.c_int, []),
 }
 
+# The test-hook build's extra symbol (include/attn_test_hooks.h).
+TEST_HOOK_SIGNATURES = {
+    "attn_fwd_withhold": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                         ctypes.c_int, ctypes.c_void_p]),
+}
+
 _lib = None
 _selftest = None
+_test_hooks = None
 
 
 class AttnError(RuntimeError):
@@ -73,6 +79,22 @@ def lib():
             fn.argtypes = args
         _lib = handle
     return _lib
+
+
+def test_hooks_lib():
+    """libattn_testhooks.so (the kernels with -DATTN_TEST_HOOKS), for the tests of the bounded
+    waits. It carries its own copy of the device status word: read it through this handle."""
+    global _test_hooks
+    if _test_hooks is None:
+        if not os.path.exists(TEST_HOOKS_PATH):
+            raise RuntimeError(f"{TEST_HOOKS_PATH} is missing: build it first")
+        h = ctypes.CDLL(TEST_HOOKS_PATH)
+        for name, (res, args) in {**SIGNATURES, **TEST_HOOK_SIGNATURES}.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _test_hooks = h
+    return _test_hooks
 
 
 def selftest_lib():

@@ -37,8 +37,9 @@
 // The only other barriers are the CTA-wide ones at entry and exit, and each softmax
 // warpgroup's per-tile named barrier: a warp that gives up records the iteration in shared
 // memory before it joins that barrier, and the other three leave at the same iteration.
-// attn_fwd_withhold runs this path on purpose: its producer skips one K/V token, so the waits
-// on that token run out.
+// The test-hook build (-DATTN_TEST_HOOKS, libattn_testhooks.so) adds attn_fwd_withhold, which
+// runs this path on purpose: its producer skips one K/V token, so the waits on that token run
+// out. The product build has neither that entry point nor the parameter.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -50,6 +51,9 @@
 #include <mutex>
 
 #include "attn.h"
+#ifdef ATTN_TEST_HOOKS
+#include "attn_test_hooks.h"
+#endif
 #include "ptx.cuh"
 
 namespace gb300 {
@@ -133,8 +137,17 @@ struct Params {
   int n_qp;         // ceil(S / 256): CTAs per (b, h)
   int BH;           // B * H
   float scale_log2; // scale * log2(e)
+#ifdef ATTN_TEST_HOOKS
   int withhold;     // K/V token the producer never loads (bounded-wait test hook), -1: none
+#endif
 };
+
+// Whether the producer skips token t (only the test-hook build ever does).
+#ifdef ATTN_TEST_HOOKS
+#define ATTN_WITHHELD(p, t) ((t) == (p).withhold)
+#else
+#define ATTN_WITHHELD(p, t) false
+#endif
 
 struct Ctl {
   uint32_t bar0;                  // smem address of barrier 0
@@ -304,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = kv_smem + s * kTileBytes;
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         const int row = (t >> 1) * kBlock;
-        if (t != p.withhold) {
+        if (!ATTN_WITHHELD(p, t)) {
           mbar_arrive_expect_tx(bar, kTileBytes);
           tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, keep);
           tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
         for (int q = 0; q < 2; ++q) wait_slow(c, kBarQFull + q, 0, kRoleLoad, false, kDrainLimitNs);
         for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
-          if (t != p.withhold)
+          if (!ATTN_WITHHELD(p, t))
             wait_slow(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleLoad, false, kDrainLimitNs);
       }
     }
@@ -799,6 +812,8 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
               overlaps(lse, lse_bytes, v, vb) || overlaps(lse, lse_bytes, o, ob)))
     return ATTN_ERR_INVALID_ARG;
 
+  if (check_only == 2) return ATTN_OK;  // arguments only, no CUDA call
+
   int dev = -1;
   const int status = prepare_device(&dev);
   if (status != ATTN_OK) return status;
@@ -818,7 +833,9 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   prm.n_qp = static_cast<int>(n_qp);
   prm.BH = static_cast<int>(BH);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+#ifdef ATTN_TEST_HOOKS
   prm.withhold = withhold;
+#endif
 
   const dim3 grid(static_cast<unsigned>(BH * n_qp));
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
@@ -855,12 +872,14 @@ int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float*
   return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, -1, 0, stream);
 }
 
+#ifdef ATTN_TEST_HOOKS
 int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                       int S, int D, float scale, int token, void* stream) {
   if (token < 0) return ATTN_ERR_INVALID_ARG;
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
   return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 0, token, 0, stream);
 }
+#endif
 
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d,
                   void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int S, int D, float scale,
@@ -869,10 +888,17 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
   if ((lse_h == nullptr) != (lse_d == nullptr)) return ATTN_ERR_INVALID_ARG;
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
   // Everything the kernel launch would reject is rejected before any copy is enqueued.
-  int r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 1, stream);
+  int r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 2, stream);
   if (r != ATTN_OK) return r;
   const size_t bytes = static_cast<size_t>(B) * H * S * D * 2;
   const size_t lse_bytes = static_cast<size_t>(B) * H * S * 4;
+  // q_d, k_d and v_d are copy destinations here (the kernel alone may read aliased inputs):
+  // one copy would overwrite another's data.
+  if (gb300::overlaps(q_d, bytes, k_d, bytes) || gb300::overlaps(q_d, bytes, v_d, bytes) ||
+      gb300::overlaps(k_d, bytes, v_d, bytes))
+    return ATTN_ERR_INVALID_ARG;
+  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 1, stream);
+  if (r != ATTN_OK) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(q_d, q_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(k_d, k_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||

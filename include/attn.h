@@ -126,14 +126,16 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
  *   o_h           : HOST pointer, BF16 [B, H, S, D], written by the copy-out.
  *   lse_h         : HOST pointer, fp32 [B, H, S], or NULL (then lse_d must be NULL too).
  *   q_d .. lse_d  : DEVICE buffers of the same shapes, owned by the caller, with attn_fwd's
- *                   alignment and no-overlap rules; the library allocates nothing.
+ *                   alignment rules; the library allocates nothing. No two of the five may
+ *                   overlap: unlike attn_fwd's inputs, q_d, k_d and v_d are written (by the
+ *                   copy-in), so they may not alias one another either.
  *   causal        : 0 = attn_fwd, 1 = attn_fwd_causal.
  * Host buffers should be page-locked (cudaHostAlloc, or a pinned torch tensor) for the copies
  * to run asynchronously and overlap other streams; pageable memory still works, with the
  * CUDA runtime's staging.
  * Errors: every check attn_fwd makes is made before anything is enqueued, plus NULL host
- * pointers and an lse_h / lse_d mismatch (ATTN_ERR_INVALID_ARG); a failed copy is
- * ATTN_ERR_LAUNCH.
+ * pointers, an lse_h / lse_d mismatch and overlapping q_d / k_d / v_d (ATTN_ERR_INVALID_ARG);
+ * a failed copy is ATTN_ERR_LAUNCH.
  */
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
@@ -155,20 +157,6 @@ const char* attn_status_string(int status);
  * issue, 4 = O correction; barrier = the index of the mbarrier whose wait ran out.
  */
 int attn_device_status(unsigned int* word, int reset);
-
-/*
- * attn_fwd_withhold -- test hook for the bounded waits. Runs attn_fwd (dense, rebase
- * threshold 0) except that every CTA's TMA producer skips K/V token `token` (token 2i is
- * K tile i, token 2i+1 is V tile i, tiles of 128 keys), so the waits that need it never
- * complete. About two seconds after launch the first such wait gives up and records its
- * status word (see attn_device_status); every CTA then drains its own loads and MMAs, frees
- * its tensor memory and exits, and the context stays usable. O and lse are left undefined.
- *
- *   token : 0 <= token < 2 * ceil(S / 128), else ATTN_ERR_INVALID_ARG.
- * Other arguments, errors and ownership as attn_fwd. Nothing a user needs calls this.
- */
-int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse,
-                      int B, int H, int S, int D, float scale, int token, void* stream);
 
 /* Library version, (major << 16) | minor. */
 int attn_version(void);

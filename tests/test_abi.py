@@ -3,6 +3,7 @@ arguments on the host before any CUDA call. CPU only (no compute calls)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -31,8 +32,38 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_causal", "attn_fwd_ex",
-                                  "attn_fwd_host", "attn_fwd_strided", "attn_fwd_withhold",
-                                  "attn_status_string", "attn_version"]
+                                  "attn_fwd_host", "attn_fwd_strided", "attn_status_string", "attn_version"]
+
+
+def test_product_library_exports_exactly_the_product_abi(lib):
+    """libattn.so's dynamic symbol table holds the entry points of attn.h and no other attn_*
+    function: the test hook and the trace calls live in their own builds."""
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm is not available")
+    exported = sorted({ln.split()[-1] for ln in out.stdout.splitlines()
+                       if ln.split() and ln.split()[-1].startswith("attn_")})
+    assert exported == declared_symbols()
+
+
+def test_test_hook_build_exports_both_headers(lib):
+    from dense_attention_forward_gb300 import build
+    hook_header = os.path.join(ROOT, "include", "attn_test_hooks.h")
+    hook_syms = sorted(set(re.findall(r"^\s*int\s+(attn_\w+)\s*\(", open(hook_header).read(), re.M)))
+    assert hook_syms == ["attn_fwd_withhold"] == sorted(_lib.TEST_HOOK_SIGNATURES)
+    hl = ctypes.CDLL(build.build_test_hooks())
+    for name in declared_symbols() + hook_syms:
+        assert hasattr(hl, name), name
+    assert not hasattr(lib, "attn_fwd_withhold")
+
+
+def test_check_device_status_decodes_a_timeout_word(monkeypatch):
+    # The binding's decoding of a non-zero status word (of the form the kernel writes when a
+    # bounded wait runs out) into ATTN_ERR_TIMEOUT naming the role and the barrier.
+    monkeypatch.setattr(_lib, "device_status", lambda reset=True: 0xA77E0000 | (3 << 8) | 7)
+    with pytest.raises(attn.AttnError) as e:
+        _lib.check_device_status()
+    assert e.value.status == 6 and "softmax" in str(e.value) and "mbarrier 7" in str(e.value)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -135,13 +166,16 @@ def test_causal_argument_errors(lib, kw, expected):
 @pytest.mark.parametrize("S,token,expected", [
     (256, -1, 1), (256, -5, 1), (256, 4, 1), (300, 6, 1), (256, 3, 4), (300, 5, 4),
 ])
-def test_withhold_token_range(lib, S, token, expected):
+def test_withhold_token_range(S, token, expected):
     """The test hook accepts only a token the CTAs walk (2 per 128-key tile); a valid call
     reaches the device check, which fails here without a GPU."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    assert lib.attn_fwd_withhold(Q, K, V, O, L, 1, 1, S, 128, 0.088, token, None) == expected
+    from dense_attention_forward_gb300 import build
+    build.build_test_hooks()
+    hl = _lib.test_hooks_lib()
+    assert hl.attn_fwd_withhold(Q, K, V, O, L, 1, 1, S, 128, 0.088, token, None) == expected
 
 
 # Fake host addresses (never dereferenced: every case fails before a copy is enqueued).
@@ -152,6 +186,8 @@ QH, KH, VH, OH, LH = 0x61000000, 0x62000000, 0x63000000, 0x64000000, 0x65000000
     (dict(q_h=None), 1), (dict(k_h=None), 1), (dict(v_h=None), 1), (dict(o_h=None), 1),
     (dict(lse_h=None), 1), (dict(lse_d=None), 1), (dict(D=64), 2), (dict(S=0), 1), (dict(causal=2), 1),
     (dict(o_d=Q), 1), (dict(q_d=Q + 8), 3),
+    # q_d, k_d, v_d are copy destinations: no two may overlap (256 rows x 256 B = 64 KB each)
+    (dict(k_d=Q), 1), (dict(v_d=K), 1), (dict(v_d=Q + 65536 - 16), 1), (dict(k_d=V - 65536 + 16), 1),
 ])
 def test_host_entry_argument_errors(lib, kw, expected):
     a = dict(q_h=QH, k_h=KH, v_h=VH, o_h=OH, lse_h=LH, q_d=Q, k_d=K, v_d=V, o_d=O, lse_d=L,
@@ -168,6 +204,10 @@ def test_host_entry_without_lse_and_without_device(lib):
         pytest.skip("a GPU is present")
     # Valid arguments reach the device check (nothing is enqueued without a GPU).
     assert lib.attn_fwd_host(QH, KH, VH, OH, None, Q, K, V, O, None, 1, 1, 256, 128, 0.088, 0, None) == 4
+    # Adjacent (touching, not overlapping) device buffers are valid too.
+    n = 256 * 128 * 2
+    assert lib.attn_fwd_host(QH, KH, VH, OH, None, Q, Q + n, Q + 2 * n, O, None, 1, 1, 256, 128, 0.088, 0,
+                             None) == 4
 
 
 def test_no_device_is_reported(lib):
@@ -198,3 +238,24 @@ def test_python_wrapper_rejects_cpu_and_wrong_dtype():
     y = torch.zeros(1, 1, 8, 128, dtype=torch.float32)
     with pytest.raises((TypeError, ValueError)):
         attn.fwd(y, y, y)
+
+
+def test_fwd_host_rejects_bad_device_buffers():
+    """fwd_host checks a caller-supplied dev tuple before any C call: count, shape, dtype,
+    contiguity, then that the buffers are CUDA tensors."""
+    import torch
+    B, H, S, D = 1, 2, 40, 128
+    q = torch.zeros(B, H, S, D, dtype=torch.bfloat16)
+    good = [torch.empty(B, H, S, D, dtype=torch.bfloat16) for _ in range(4)] + [torch.empty(B, H, S)]
+    bad = {
+        "count": tuple(good[:4]),
+        "shape": (torch.empty(B, H, S - 1, D, dtype=torch.bfloat16),) + tuple(good[1:]),
+        "dtype": tuple(good[:3]) + (torch.empty(B, H, S, D),) + (good[4],),
+        "lse shape": tuple(good[:4]) + (torch.empty(B, H, S + 1),),
+        "contiguity": (torch.empty(B, S, H, D, dtype=torch.bfloat16).transpose(1, 2),) + tuple(good[1:]),
+        "not cuda": tuple(good),
+    }
+    for what, dev in bad.items():
+        with pytest.raises(ValueError):
+            attn.fwd_host(q, q, q, out=torch.empty(B, H, S, D, dtype=torch.bfloat16),
+                          lse=torch.empty(B, H, S), dev=dev)
