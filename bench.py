@@ -15,7 +15,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -33,18 +32,55 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
-# valid only for the kernel source it was taken on (hash of the CUDA sources).
-TRAFFIC = {"s4k": (246194944, "ecaf6eb2a7824564")}  # ncu: 201,383,680 B read + 44,811,264 B written
+# keyed by sweep entry; each is valid only for the kernel source it was taken on (hash of the
+# kernel's CUDA sources), and is reported as null otherwise.
+TRAFFIC: dict[str, tuple[int, str]] = {}
+
+# Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64
+# cycles, measured on this part with isolated MMA chains.
+FLOP_PER_CLK_SM = 8192
+# The nominal dense (no 2:4 sparsity) BF16 rate of one GB300, PFLOP/s.
+NOMINAL_BF16_TFLOPS = 2250.0
+KERNEL_SOURCES = ("attn_fwd.cu", "ptx.cuh")
 
 
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_attention_forward_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")) and name != "selftest.cu":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def step_stats(times_ms):
+    """mean / median / min / max of per-step kernel times (ms)."""
+    return {"mean": round(sum(times_ms) / len(times_ms), 5), "median": round(statistics.median(times_ms), 5),
+            "min": round(min(times_ms), 5), "max": round(max(times_ms), 5)}
+
+
+def roofline(flops, ms, peak, sm_count, sm_mhz, traffic=None):
+    """Achieved TFLOP/s per launch against three denominators: the measured cuBLAS BF16 burst
+    (`peak`, the headline fraction), the nominal dense BF16 figure, and the SM count x the
+    per-SM MMA rate x the SM clock sampled during the run."""
+    achieved = flops / (ms * 1e-3) / 1e12
+    out = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+           "frac": round(achieved / peak, 4), "traffic": traffic,
+           "peak_nominal": NOMINAL_BF16_TFLOPS, "frac_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4)}
+    if sm_mhz:
+        clk_peak = sm_count * FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
+        out["peak_clock"] = round(clk_peak, 1)
+        out["frac_clock"] = round(achieved / clk_peak, 4)
+    return out
+
+
+def config_of(w: wl.Workload, world: int, causal: bool = False) -> dict:
+    """The workload description both arms print."""
+    return {"workload": w.label(), "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": causal,
+            "scale": w.scale, "inputs": "seeded N(0,1) BF16" + (f", Q and K x{w.qk_gain:g}" if w.qk_gain != 1 else ""),
+            "l2": "flushed between timed steps (256 MB write)" + (
+                "; inputs larger than L2" if 3 * w.rows * w.D * 2 > 129e6 else ""),
+            "parallelism": f"replicas x{world}"}
 
 
 def load_peaks():
@@ -178,7 +214,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": warm, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.label(), "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": False},
+        "config": config_of(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -214,6 +250,7 @@ def run_gpu(args, w):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     q, k, v = (t.to(dev) for t in wl.make_qkv(w))
     o = torch.empty_like(q)
@@ -238,6 +275,7 @@ def run_gpu(args, w):
     kern_ms = max_over_ranks(kern_ms, dist, dev)
     value = job_throughput(w.flops, kern_ms, world)
     status = attn.device_status(reset=True)
+    clocks = clk.summary()
 
     # ---- end to end: the library's host-to-host call (attn_fwd_host) every step: pinned host
     # q, k, v -> device, the kernel, device -> pinned host o and lse. Steps alternate between
@@ -257,6 +295,9 @@ def run_gpu(args, w):
     for kstep in range(4):
         e2e_step(kstep)
     barrier()
+    for b in range(2):  # poison the outputs: the timed steps must write them again
+        oh[b].fill_(float("nan"))
+        lh[b].fill_(float("nan"))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e0.record(stream)
@@ -273,31 +314,44 @@ def run_gpu(args, w):
     e2e_value = job_throughput(w.flops, e2e_ms, world)
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    # The timed end-to-end steps computed what the device-resident steps did, bit for bit, and
+    # no bounded wait gave up on the way.
+    e2e_status = attn.device_status(reset=True)
+    last = (e2e_steps - 1) & 1
+    o_dev, lse_dev = o.cpu(), lse.cpu()
+    e2e_match = bool(torch.equal(oh[last], o_dev) and torch.equal(lh[last], lse_dev) and
+                     torch.equal(oh[last ^ 1], o_dev) and torch.equal(lh[last ^ 1], lse_dev))
+    if e2e_status != 0 or not e2e_match:
+        raise RuntimeError(f"end-to-end steps: status word {e2e_status:#x}, outputs equal to the "
+                           f"device-resident call: {e2e_match}")
+
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sm_mhz = clocks.get("sm_mhz")
+
+    def traffic_of(name):
+        rec = TRAFFIC.get(name)
+        return rec[0] if (rec and rec[1] == source_hash()) else None
 
     # ---- other workloads of the same metric (single GPU, same method, fewer steps)
     sweep = {}
     if not args.no_sweep:
-        for name in args.sweep:
-            if name == w.name:
+        for name, causal in [(n, False) for n in args.sweep] + [(n, True) for n in args.causal_sweep]:
+            if name == w.name and not causal:
                 continue
             ws = wl.ALL[name]
             qs, ks, vs = (t.to(dev) for t in wl.make_qkv(ws))
             os_, ls_ = torch.empty_like(qs), torch.empty((ws.B, ws.H, ws.S), device=dev)
-            ts = time_gpu(attn, torch, ws, qs, ks, vs, os_, ls_, args.sweep_steps, 3, flush, stream)
-            ms = sum(ts) / len(ts)
-            sweep[name] = {"workload": ws.label(), "ms": round(ms, 4),
-                           "tflops": round(ws.flops / (ms * 1e-3) / 1e12, 1)}
-            del qs, ks, vs, os_, ls_
-        # The causal variant (query i sees keys j <= i), FLOPs counted as 2*B*H*S^2*D.
-        for name in args.causal_sweep:
-            ws = wl.ALL[name]
-            qs, ks, vs = (t.to(dev) for t in wl.make_qkv(ws))
-            os_, ls_ = torch.empty_like(qs), torch.empty((ws.B, ws.H, ws.S), device=dev)
             ts = time_gpu(attn, torch, ws, qs, ks, vs, os_, ls_, args.sweep_steps, 3, flush, stream,
-                          causal=True)
+                          causal=causal)
             ms = sum(ts) / len(ts)
-            sweep[name + "_causal"] = {"workload": ws.label() + " causal", "ms": round(ms, 4),
-                                       "tflops": round(ws.flops / 2 / (ms * 1e-3) / 1e12, 1)}
+            # Causal FLOPs are counted as half the dense ones, 2*B*H*S^2*D.
+            flops = ws.flops / 2 if causal else ws.flops
+            key = name + ("_causal" if causal else "")
+            sweep[key] = {"workload": ws.label() + (" causal" if causal else ""), "ms": round(ms, 4),
+                          "step_ms": step_stats(ts), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                          "tflops_median": round(flops / (statistics.median(ts) * 1e-3) / 1e12, 1),
+                          "roofline": roofline(flops, ms, peak, sm_count, sm_mhz, traffic_of(key))}
             del qs, ks, vs, os_, ls_
         status |= attn.device_status(reset=True)
 
@@ -306,31 +360,27 @@ def run_gpu(args, w):
             dist.destroy_process_group()
         return
 
-    peaks, peaks_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved = w.flops / (kern_ms * 1e-3) / 1e12  # per GPU, per launch
-    trec = TRAFFIC.get(w.name)
-    traffic = trec[0] if (trec and trec[1] == source_hash()) else None
-    for name, rec in sweep.items():
-        rec["frac_of_peak"] = round(rec["tflops"] / peak, 4)
-
+    rf = roofline(w.flops, kern_ms, peak, sm_count, sm_mhz, traffic_of(w.name))
+    rf["peak_source"] = f"{peaks_src} bf16_tflops (burst, cuBLAS 8192^3)"
+    rf["peak_nominal_source"] = "nominal dense BF16 rate of one GB300 (no 2:4 sparsity)"
+    rf["peak_clock_source"] = (f"{sm_count} SMs x {FLOP_PER_CLK_SM} FLOP/clk (one M128 N128 K16 MMA per 64 "
+                               "cycles) x median sampled SM clock")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": round(kern_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.label(), "B": w.B, "H": w.H, "S": w.S, "D": w.D,
-                   "causal": False, "scale": w.scale, "inputs": "seeded N(0,1) BF16",
-                   "l2": "flushed between timed steps (256 MB write); inputs 268 MB > L2",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peaks_src} bf16_tflops (burst, cuBLAS 8192^3)"},
+        "config": config_of(w, world),
+        "step_ms": step_stats(times),
+        "value_median": round(job_throughput(w.flops, statistics.median(times), world), 2),
+        "value_best": round(job_throughput(w.flops, min(times), world), 2),
+        "roofline": rf,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "schedule": "attn_fwd_host per step (copy-in, kernel, copy-out), steps alternating over 2 streams with their own buffers"},
+                "schedule": "attn_fwd_host per step (copy-in, kernel, copy-out), steps alternating over 2 streams with their own buffers",
+                "device_status": e2e_status, "outputs_equal_device_call": e2e_match},
         "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
         "device_status": status,
         "sweep": sweep,

@@ -38,11 +38,11 @@ def test_causal_first_row_is_exactly_v0():
     assert np.max(np.abs(lse[:, :, 0] - s00)) < 1e-4
 
 
-@pytest.mark.parametrize("name", ["s4k", "ragged"])
-def test_causal_full_size_sampled(name):
+@pytest.mark.parametrize("name,thr", [("s4k", 0), ("s8k", 0), ("s16k", 0), ("ragged", 0), ("s16k", 8)])
+def test_causal_full_size_sampled(name, thr):
     w = wl.ALL[name]
     q, k, v = wl.make_qkv(w)
-    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale, 0, causal=True)
+    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale, thr, causal=True)
     rng = np.random.default_rng(w.seed)
     rows = set(range(0, 130)) | set(range(250, 262)) | set(range(w.S - 140, w.S))
     rows |= set(rng.integers(0, w.S, size=64).tolist())
