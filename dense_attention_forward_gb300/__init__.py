@@ -11,7 +11,7 @@ import math
 from ._lib import (AttnError, attn_fwd, attn_fwd_ex, attn_fwd_strided, check_device_status,  # noqa: F401
                    device_status, lib)
 
-__all__ = ["fwd", "fwd_host", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "check_device_status",
+__all__ = ["fwd", "fwd_host", "fwd_host_noalloc", "attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "device_status", "check_device_status",
            "AttnError", "lib"]
 
 
@@ -141,3 +141,48 @@ def fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, dev=None, 
     if st != 0:
         raise AttnError(st, "attn_fwd_host")
     return out, lse, dev
+
+
+def fwd_host_noalloc(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False,
+                     stream=None):
+    """attn_fwd_host_noalloc: host q, k, v in, host o and lse out, staged through the library's
+    own fixed device array, so nothing is allocated on the device (for callers that may not
+    allocate device memory). B * H * S must not exceed NOALLOC_MAX_ROWS (32768).
+
+    q, k, v: contiguous CPU bfloat16 tensors [B, H, S, 128]; out / lse: contiguous CPU tensors
+    for o (bfloat16) and lse (float32), plain CPU tensors if not given; lse=False skips lse.
+    Calls share the array: order them on one stream. The call only enqueues work on `stream`
+    (default: the current stream); synchronise before reading out / lse. Returns (out, lse).
+    """
+    import torch
+    from ._lib import NOALLOC_MAX_ROWS
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU bfloat16 tensor")
+        if t.dim() != 4 or tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must be [B, H, S, D] like q")
+    B, H, S, D = q.shape
+    if B * H * S > NOALLOC_MAX_ROWS:
+        raise ValueError(f"B*H*S = {B * H * S} exceeds the {NOALLOC_MAX_ROWS} rows of the library's "
+                         "staging array; use fwd_host with device buffers of your own")
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32)
+    elif lse is False:
+        lse = None
+    for name, t, dt, shape in (("out", out, torch.bfloat16, (B, H, S, D)), ("lse", lse, torch.float32, (B, H, S))):
+        if t is None:
+            continue
+        if t.is_cuda or t.dtype != dt or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of shape {shape}")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    with torch.cuda.device(stream.device):
+        st = lib().attn_fwd_host_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr() if lse is not None else None, B, H, S, D,
+                                         float(scale if scale is not None else 1.0 / math.sqrt(D)),
+                                         int(bool(causal)), stream.cuda_stream)
+    if st != 0:
+        raise AttnError(st, "attn_fwd_host_noalloc")
+    return out, lse

@@ -10,6 +10,9 @@ SELFTEST_PATH = os.path.join(PKG, "libattn_selftest.so")
 TEST_HOOKS_PATH = os.path.join(PKG, "libattn_testhooks.so")
 
 ATTN_OK = 0
+# Rows (B * H * S) the library's own staging array holds for attn_fwd_host_noalloc; the same
+# number as ATTN_NOALLOC_MAX_ROWS in include/attn.h.
+NOALLOC_MAX_ROWS = 32768
 STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED_DIM",
     3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_UNSUPPORTED_DEVICE", 5: "ATTN_ERR_LAUNCH",
@@ -39,6 +42,8 @@ SIGNATURES = {
                                        ctypes.c_void_p]),
     "attn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_int] * 4 +
                       [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_host_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
+                              [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
     "attn_version": (ctypes.c_int, []),

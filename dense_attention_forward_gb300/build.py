@@ -35,7 +35,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",
          "-I" + INCLUDE, "-I" + CSRC, "--cudart", "static"]
 
-KERNEL_SOURCES = ["attn_fwd.cu"]
+KERNEL_SOURCES = ["attn_fwd.cu", "attn_noalloc.cu"]
 
 # target -> (sources, extra defines)
 TARGETS = {

@@ -141,6 +141,35 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
                   void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
                   int B, int H, int S, int D, float scale, int causal, void* stream);
 
+/*
+ * attn_fwd_host_noalloc -- attn_fwd_host for callers that cannot allocate device memory (code
+ * that may not call cudaMalloc because another allocator owns the device memory of the process,
+ * or that runs where allocations are forbidden). The pages have no counterpart: this is a
+ * convenience of this library's boundary, not a step of the method.
+ *
+ * The device staging that attn_fwd_host takes from its caller (q_d .. lse_d) is instead a fixed
+ * array inside the library, ATTN_NOALLOC_MAX_ROWS rows of q, k, v, o and lse (33,685,504 bytes),
+ * held on every GPU where the library's device code is loaded until the process exits. The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *   q_h .. lse_h, B, H, S, D, scale, causal, stream : as attn_fwd_host (lse_h may be NULL).
+ *   B * H * S must not exceed ATTN_NOALLOC_MAX_ROWS (e.g. B = 1, H = 8, S = 4096), else
+ *   ATTN_ERR_INVALID_ARG before anything is enqueued.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the array's device
+ * address with cudaGetSymbolAddress, which may load the library's device code; make that first
+ * call before any stream capture. Later calls only enqueue the copies and the kernel.
+ * Sharing: every call uses the same array, which keeps the last call's contents; nothing in it
+ * needs clearing, since each call overwrites whatever it reads. Calls whose work overlaps on
+ * the GPU (different streams, not ordered by events or synchronisation) race on the array and
+ * corrupt each other's results: order them, e.g. one stream.
+ * Errors: as attn_fwd_host; ATTN_ERR_UNSUPPORTED_DEVICE also when the current device is not
+ * sm_103, ATTN_ERR_LAUNCH when the array's address cannot be obtained.
+ */
+#define ATTN_NOALLOC_MAX_ROWS 32768
+int attn_fwd_host_noalloc(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                          int B, int H, int S, int D, float scale, int causal, void* stream);
+
 /* A short, static, human-readable description of a status code. Never NULL. */
 const char* attn_status_string(int status);
 

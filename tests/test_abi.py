@@ -32,7 +32,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == ["attn_device_status", "attn_fwd", "attn_fwd_causal", "attn_fwd_ex",
-                                  "attn_fwd_host", "attn_fwd_strided", "attn_status_string", "attn_version"]
+                                  "attn_fwd_host", "attn_fwd_host_noalloc", "attn_fwd_strided",
+                                  "attn_status_string", "attn_version"]
 
 
 def test_product_library_exports_exactly_the_product_abi(lib):
