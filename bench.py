@@ -34,7 +34,10 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
 # keyed by sweep entry; each is valid only for the kernel source it was taken on (hash of the
 # kernel's CUDA sources), and is reported as null otherwise.
-TRAFFIC: dict[str, tuple[int, str]] = {}
+TRAFFIC: dict[str, tuple[int, str]] = {
+    "s4k": (246282752, "e274d76ed600f58f"),   # 201,382,912 B read + 44,899,840 B written
+    "s16k": (248252160, "e274d76ed600f58f"),  # 201,380,096 B read + 46,872,064 B written
+}
 
 # Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64
 # cycles, measured on this part with isolated MMA chains.
