@@ -35,8 +35,9 @@ L2_FLUSH_BYTES = 256 << 20
 # keyed by sweep entry; each is valid only for the kernel source it was taken on (hash of the
 # kernel's CUDA sources), and is reported as null otherwise.
 TRAFFIC: dict[str, tuple[int, str]] = {
-    "s4k": (246282752, "e274d76ed600f58f"),   # 201,382,912 B read + 44,899,840 B written
-    "s16k": (248252160, "e274d76ed600f58f"),  # 201,380,096 B read + 46,872,064 B written
+    "s4k": (246420992, "63ed13ec744bee37"),         # 201,383,168 B read + 45,037,824 B written
+    "s16k": (245436928, "63ed13ec744bee37"),        # 201,375,744 B read + 44,061,184 B written
+    "s4k_causal": (244635904, "63ed13ec744bee37"),  # 201,544,960 B read + 43,090,944 B written
 }
 
 # Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64
@@ -172,25 +173,28 @@ def job_throughput(flops_per_rank: float, ms: float, world: int) -> float:
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
-def time_oracle(w: wl.Workload, q, k, v, budget_s: float, min_chunks: int = 1):
+def time_oracle(w: wl.Workload, q, k, v, budget_s: float, min_chunks: int = 1, causal: bool = False):
     """Time the oracle on row chunks (all heads) until `budget_s` has elapsed. Returns
-    (TFLOPS, seconds, rows_per_head, cores)."""
+    (TFLOPS, seconds, rows_per_head, cores). Causal work is counted as the keys each row sees
+    (4*D FLOP per key), which sums to the 2*B*H*S^2*D convention over a whole call."""
     from oracle import attn_ref as ref
     qf, kf, vf = wl.to_f64(q), wl.to_f64(k), wl.to_f64(v)
     chunk = 32
     rows_done = 0
+    keys_done = 0
     t0 = time.perf_counter()
     i = 0
     while True:
         r0 = (i * chunk) % w.S
         rows = list(range(r0, min(w.S, r0 + chunk)))
-        ref.attention_rows(qf, kf, vf, w.scale, rows)
+        ref.attention_rows(qf, kf, vf, w.scale, rows, causal=causal)
         rows_done += len(rows)
+        keys_done += sum(r + 1 for r in rows) if causal else len(rows) * w.S
         i += 1
         el = time.perf_counter() - t0
         if el >= budget_s and i >= min_chunks:
             break
-    flops = 4.0 * w.B * w.H * rows_done * w.S * w.D
+    flops = 4.0 * w.B * w.H * keys_done * w.D
     return flops / el / 1e12, el, rows_done, os.cpu_count()
 
 
@@ -201,10 +205,10 @@ def run_reference(args, w):
     q, k, v = wl.make_qkv(w)
     warm = max(args.warmup, 3)
     for _ in range(warm):
-        time_oracle(w, q, k, v, budget_s=0.0)
+        time_oracle(w, q, k, v, budget_s=0.0, causal=args.causal)
     rates, secs, rows = [], 0.0, 0
     for _ in range(args.steps):
-        r, el, nrows, cores = time_oracle(w, q, k, v, budget_s=args.ref_step_seconds)
+        r, el, nrows, cores = time_oracle(w, q, k, v, budget_s=args.ref_step_seconds, causal=args.causal)
         rates.append(r)
         secs += el
         rows += nrows
@@ -217,7 +221,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": warm, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": config_of(w, world),
+        "config": config_of(w, world, args.causal),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -271,12 +275,13 @@ def run_gpu(args, w):
     barrier()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        times = time_gpu(attn, torch, w, q, k, v, o, lse, args.steps, warm, flush, stream)
+        times = time_gpu(attn, torch, w, q, k, v, o, lse, args.steps, warm, flush, stream, causal=args.causal)
         barrier()
         t_wall = time.perf_counter() - t_wall0
     kern_ms = sum(times) / len(times)
     kern_ms = max_over_ranks(kern_ms, dist, dev)
-    value = job_throughput(w.flops, kern_ms, world)
+    flops = w.flops / 2 if args.causal else w.flops  # causal: 2*B*H*S^2*D
+    value = job_throughput(flops, kern_ms, world)
     status = attn.device_status(reset=True)
     clocks = clk.summary()
 
@@ -293,7 +298,8 @@ def run_gpu(args, w):
 
     def e2e_step(kstep):
         b = kstep & 1
-        attn.fwd_host(qh, kh, vh, w.scale, out=oh[b], lse=lh[b], dev=bufs[b], stream=streams[b])
+        attn.fwd_host(qh, kh, vh, w.scale, out=oh[b], lse=lh[b], dev=bufs[b], stream=streams[b],
+                      causal=args.causal)
 
     for kstep in range(4):
         e2e_step(kstep)
@@ -314,7 +320,7 @@ def run_gpu(args, w):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    e2e_value = job_throughput(w.flops, e2e_ms, world)
+    e2e_value = job_throughput(flops, e2e_ms, world)
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
     # The timed end-to-end steps computed what the device-resident steps did, bit for bit, and
@@ -340,7 +346,7 @@ def run_gpu(args, w):
     sweep = {}
     if not args.no_sweep:
         for name, causal in [(n, False) for n in args.sweep] + [(n, True) for n in args.causal_sweep]:
-            if name == w.name and not causal:
+            if name == w.name and causal == args.causal:
                 continue
             ws = wl.ALL[name]
             qs, ks, vs = (t.to(dev) for t in wl.make_qkv(ws))
@@ -349,12 +355,12 @@ def run_gpu(args, w):
                           causal=causal)
             ms = sum(ts) / len(ts)
             # Causal FLOPs are counted as half the dense ones, 2*B*H*S^2*D.
-            flops = ws.flops / 2 if causal else ws.flops
+            sflops = ws.flops / 2 if causal else ws.flops
             key = name + ("_causal" if causal else "")
             sweep[key] = {"workload": ws.label() + (" causal" if causal else ""), "ms": round(ms, 4),
-                          "step_ms": step_stats(ts), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
-                          "tflops_median": round(flops / (statistics.median(ts) * 1e-3) / 1e12, 1),
-                          "roofline": roofline(flops, ms, peak, sm_count, sm_mhz, traffic_of(key))}
+                          "step_ms": step_stats(ts), "tflops": round(sflops / (ms * 1e-3) / 1e12, 1),
+                          "tflops_median": round(sflops / (statistics.median(ts) * 1e-3) / 1e12, 1),
+                          "roofline": roofline(sflops, ms, peak, sm_count, sm_mhz, traffic_of(key))}
             del qs, ks, vs, os_, ls_
         status |= attn.device_status(reset=True)
 
@@ -363,7 +369,7 @@ def run_gpu(args, w):
             dist.destroy_process_group()
         return
 
-    rf = roofline(w.flops, kern_ms, peak, sm_count, sm_mhz, traffic_of(w.name))
+    rf = roofline(flops, kern_ms, peak, sm_count, sm_mhz, traffic_of(w.name + ("_causal" if args.causal else "")))
     rf["peak_source"] = f"{peaks_src} bf16_tflops (burst, cuBLAS 8192^3)"
     rf["peak_nominal_source"] = "nominal dense BF16 rate of one GB300 (no 2:4 sparsity)"
     rf["peak_clock_source"] = (f"{sm_count} SMs x {FLOP_PER_CLK_SM} FLOP/clk (one M128 N128 K16 MMA per 64 "
@@ -373,10 +379,10 @@ def run_gpu(args, w):
         "steps": args.steps, "warmup": warm, "ms_per_step": round(kern_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": config_of(w, world),
+        "config": config_of(w, world, args.causal),
         "step_ms": step_stats(times),
-        "value_median": round(job_throughput(w.flops, statistics.median(times), world), 2),
-        "value_best": round(job_throughput(w.flops, min(times), world), 2),
+        "value_median": round(job_throughput(flops, statistics.median(times), world), 2),
+        "value_best": round(job_throughput(flops, min(times), world), 2),
         "roofline": rf,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
@@ -390,7 +396,7 @@ def run_gpu(args, w):
     }
     if not args.no_cpu_baseline and world == 1:
         qc, kc, vc = wl.make_qkv(w)
-        rate, el, rows, cores = time_oracle(w, qc, kc, vc, budget_s=args.cpu_seconds)
+        rate, el, rows, cores = time_oracle(w, qc, kc, vc, budget_s=args.cpu_seconds, causal=args.causal)
         line["cpu_baseline"] = {
             "value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle on {rows} query rows of each of the {w.B * w.H} heads of "
@@ -407,6 +413,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="s4k", choices=sorted(wl.ALL))
+    ap.add_argument("--causal", action="store_true",
+                    help="time the causal variant as the step (FLOPs counted as 2*B*H*S^2*D)")
     ap.add_argument("--sweep", nargs="*", default=["s8k", "s16k", "ragged"])
     ap.add_argument("--causal-sweep", nargs="*", default=["s4k", "s8k", "s16k"])
     ap.add_argument("--sweep-steps", type=int, default=100)

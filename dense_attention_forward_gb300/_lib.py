@@ -148,7 +148,7 @@ def device_status(reset: bool = True) -> int:
     return word.value
 
 
-_ROLES = {1: "TMA producer", 2: "MMA issue", 3: "softmax / MMA issue", 4: "O correction"}
+_ROLES = {1: "TMA producer", 2: "MMA issue", 3: "softmax", 4: "O correction"}
 
 
 def check_device_status(reset: bool = True) -> None:

@@ -7,15 +7,17 @@
 //  * Work split (Ch. 1 §ii, Ch. 5): one CTA owns two consecutive 128-row Q tiles of one
 //    (batch, head) and walks every 128-key K/V tile of that head; each K/V tile loaded into
 //    shared memory serves both Q tiles.
-//  * Loads (Ch. 3, Ch. 6): one TMA warp streams K and V as separate tokens through a
-//    kStages-slot ring of 32 KB SW128 slots; a slot is refilled once the second Q tile's
-//    S-full commit that follows its last consumer (that tile's QK for K, its PV for V) has
-//    arrived, so no MMA commit is spent on freeing slots.
-//  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 5, Ch. 7): tcgen05.mma M128 N128 K16, S_q = Q_q K^T (both
-//    K-major SW128 in shared memory) and O_q += P_q V (P from tensor memory, V MN-major
-//    SW128). Each softmax warpgroup's first thread issues its own Q tile's MMAs, PV_q(i) then
-//    QK_q(i+1), right after a named barrier shows P_q(i) stored; the two issuing threads take
-//    turns group by group so one Q tile's softmax overlaps the other's MMAs (ping-pong).
+//  * Loads (Ch. 3, Ch. 6): Q0, K0 and Q1 leave right after the barriers are initialised; one
+//    TMA warp then streams K and V as separate tokens through a kStages-slot ring of 32 KB
+//    SW128 slots; a slot is refilled once the second Q tile's S-full commit that follows its
+//    last consumer (that tile's QK for K, its PV for V) has arrived, so no MMA commit is spent
+//    on freeing slots.
+//  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 5, Ch. 7, Ch. 13): tcgen05.mma M128 N128 K16, S_q = Q_q K^T
+//    (both K-major SW128 in shared memory) and O_q += P_q V (P from tensor memory, V MN-major
+//    SW128). One warp per Q tile issues that tile's MMAs: in K/V tile i, the PV_q(i) steps of
+//    each part of P_q(i) as soon as the softmax has stored that part (the pages' "early PV"),
+//    then QK_q(i+1). The two issuing warps take turns group by group, so one Q tile's softmax
+//    overlaps the other's MMAs (ping-pong).
 //  * Softmax (Ch. 1 §B, Ch. 8, Ch. 11): 4 warps per Q tile, one thread per row, the whole
 //    128-score row in registers; base-2 exponent with scale*log2(e) folded into one factor,
 //    row max taken on raw scores; P is packed to BF16 pairs and stored over S in tensor
@@ -31,12 +33,14 @@
 //    lse = (m + log2 l) * ln 2 is written by the same threads.
 //
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
-// the first 64 columns of S_q. Warp 14 loads, warp 13 owns the TMEM allocation. Every
-// mbarrier wait is bounded (about two seconds); a CTA that gives up records the failure in a
-// device status word, drains its own TMA loads and MMAs, frees its tensor memory and exits.
-// The only other barriers are the CTA-wide ones at entry and exit, and each softmax
-// warpgroup's per-tile named barrier: a warp that gives up records the iteration in shared
-// memory before it joins that barrier, and the other three leave at the same iteration.
+// the first 64 columns of S_q. Warps 0-7 softmax, 8-11 correction, 12 and 13 MMA issue (13
+// also owns the TMEM allocation), 14 loads. Every mbarrier wait is bounded (about two
+// seconds); a CTA that gives up records the failure in a device status word, drains its own
+// TMA loads and MMAs, frees its tensor memory and exits. The only other barriers are the
+// CTA-wide ones at entry and exit, and the named barriers on which each Q tile's softmax warps
+// (arriving) meet its issuing warp (waiting), one per part of P: a softmax warp that gives up
+// records the iteration in shared memory and arrives at all of that iteration's barriers
+// before it leaves, and the issuing warp reads the record before it waits for the next ones.
 // The test-hook build (-DATTN_TEST_HOOKS, libattn_testhooks.so) adds attn_fwd_withhold, which
 // runs this path on purpose: its producer skips one K/V token, so the waits on that token run
 // out. The product build has neither that entry point nor the parameter.
@@ -49,6 +53,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "attn.h"
 #ifdef ATTN_TEST_HOOKS
@@ -64,8 +69,18 @@ constexpr int kTileBytes = kBlock * kHeadDim * 2;  // one 128x128 BF16 tile: 32 
 constexpr int kSliceBytes = kBlock * 128;        // 128 rows x 128 B: one SW128 column of atoms
 constexpr int kStages = 4;                       // K/V ring slots
 constexpr int kThreads = 512;                    // 16 warps
-constexpr int kLoadWarp = 14;
-constexpr int kMmaWarp = 13;
+constexpr int kLoadWarp = 14;                    // TMA producer
+constexpr int kIssueWarp0 = 12;                  // MMA issue for Q tile 0
+constexpr int kIssueWarp1 = 13;                  // MMA issue for Q tile 1; also owns the TMEM allocation
+constexpr int kTmemWarp = kIssueWarp1;
+// P_q(i) is stored and consumed in parts: packed BF16 pairs (TMEM columns) [kPCut[k], kPCut[k+1]).
+// A PV K16 step reads 8 of them, so every cut is a multiple of 8. A small first part lets the
+// tensor pipe start PV_q(i) early; QK_q(i+1) waits for the last part.
+constexpr int kPParts = 3;
+constexpr int kPCut[kPParts + 1] = {0, 16, 40, 64};
+constexpr int kBarP = 2;  // named barrier of part k of Q tile q: kBarP + 2k + q (0 is __syncthreads)
+constexpr int kCausalGroup = 16;                 // causal launch order: heads per group
+static_assert(kBarP + 2 * kPParts <= 16, "named barrier ids");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
 
@@ -80,8 +95,8 @@ constexpr int kBarSFull = kBarKVFull + kStages;    // [2] S_q in TMEM (MMA commi
 constexpr int kBarOSafe = kBarSFull + 2;           // [2] O_q rescaled or left as is (4 correction warps)
 constexpr int kBarOFull = kBarOSafe + 2;           // [2] last PV_q done (MMA commit)
 constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
-constexpr int kBarMmaDone = kBarStats + 2;         // [2] drain after a failure (one per issuing thread)
-constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q tile q (the other leader)
+constexpr int kBarMmaDone = kBarStats + 2;         // [2] drain after a failure (one per issuing warp)
+constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q tile q (from the other issuing warp)
 constexpr int kNumBars = kBarTurn + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -193,6 +208,11 @@ __device__ __forceinline__ void warp_arrive(const Ctl& c, int b, int lane) {
   if (lane == 0) mbar_arrive(c.bar(b));
 }
 
+// Arrival without waiting (the producer side of a named barrier).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -204,6 +224,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Calls f(integral_constant<int, 0>) ... f(integral_constant<int, N - 1>): one body per part
+// of P, with compile-time column ranges.
+template <int N, int I = 0, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<N, I + 1>(f);
+  }
+}
+
 // kRebase8: keep the row max until a tile's max exceeds it by 8 (base 2), the pages' Ch. 11
 // "skip O rescale"; P can then reach 2^8, and O is normalised by a second row sum over the
 // BF16-rounded P. Otherwise (threshold 0) the kept max is the running max, P <= 1 with the
@@ -211,8 +241,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // kCausal: query i sees keys j <= i (queries and keys share positions 0..S-1). The CTA of Q
 // tiles 2qp and 2qp+1 walks K/V tiles 0..2qp+1 only; its diagonal tiles are masked per
 // element, and Q tile 2qp runs tile 2qp+1 fully masked (P = 0) so both Q tiles keep the same
-// K/V schedule. CTAs are launched longest first (descending qp, all heads) to shorten the
-// tail of the grid.
+// K/V schedule. CTAs are launched longest first (descending qp) inside groups of heads, which
+// shortens the tail of the grid and keeps each group's K/V in L2.
 template <bool kRebase8, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -223,11 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw_addr);
 
-  const int warp = threadIdx.x >> 5;
+  // The warp index, broadcast from lane 0 so that the compiler knows it is warp-uniform: the
+  // role branches and every MMA descriptor derived from it then stay in uniform registers.
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
-  const int qp = kCausal ? p.n_qp - 1 - static_cast<int>(blockIdx.x) / p.BH
-                         : static_cast<int>(blockIdx.x) % p.n_qp;
-  const int bh = kCausal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / p.n_qp;
+  int qp, bh;
+  if constexpr (kCausal) {
+    // Heads in groups of kCausalGroup, longest CTA first inside each group: a group's K/V
+    // (16 heads x 2 MB at S = 4096) stays in L2 while its CTAs run, and the short CTAs of one
+    // group overlap the long ones of the next.
+    const int per_group = kCausalGroup * p.n_qp;
+    const int g = static_cast<int>(blockIdx.x) / per_group;
+    const int r = static_cast<int>(blockIdx.x) - g * per_group;
+    const int gh = min(kCausalGroup, p.BH - g * kCausalGroup);  // heads in this group
+    qp = p.n_qp - 1 - r / gh;
+    bh = g * kCausalGroup + r % gh;
+  } else {
+    qp = static_cast<int>(blockIdx.x) % p.n_qp;
+    bh = static_cast<int>(blockIdx.x) / p.n_qp;
+  }
   const int hh = bh % p.H, bb = bh / p.H;
   const int q0 = qp * 2 * kBlock;
   const int n = kCausal ? min(p.n_kv, 2 * qp + 2) : p.n_kv;  // K/V tiles this CTA walks
@@ -243,6 +287,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const alpha_sm = reinterpret_cast<float*>(smem + kOffAlpha);
   const uint32_t q_smem = base + kOffQ;
   const uint32_t kv_smem = base + kOffKV;
+
+  // Q tile q (two 64-column boxes) into its buffer, completion counted on its barrier.
+  auto load_q = [&](int q, uint64_t policy) {
+    const uint32_t bar = c.bar(kBarQFull + q);
+    const uint32_t dst = q_smem + q * kTileBytes;
+    mbar_arrive_expect_tx(bar, kTileBytes);
+    tma_load_4d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, hh, bb, policy);
+    tma_load_4d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, hh, bb, policy);
+  };
+  // K/V token t (K(t/2) for even t, V(t/2) for odd t) into ring slot t % kStages.
+  auto load_token = [&](int t, uint64_t policy) {
+    const uint32_t bar = c.bar(kBarKVFull + t % kStages);
+    const uint32_t dst = kv_smem + (t % kStages) * kTileBytes;
+    const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+    const int row = (t >> 1) * kBlock;
+    mbar_arrive_expect_tx(bar, kTileBytes);
+    tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, policy);
+    tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, policy);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarQFull + 0), 1);
@@ -263,8 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     reinterpret_cast<volatile int*>(smem + kOffFail)[1] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
+    // The first loads (Q0, K0, then Q1: the first QK needs only Q0 and K0) leave before the
+    // TMEM allocation and the CTA-wide barrier; the producer continues with token 1.
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    const uint64_t once = l2_policy_evict_first();  // Q: read once
+    load_q(0, once);
+    if (!ATTN_WITHHELD(p, 0)) load_token(0, l2_policy_evict_last());
+    load_q(1, once);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kTmemWarp) {
     tmem_alloc(base + kOffTmemSlot, 512);
     tmem_relinquish();
   }
@@ -273,35 +344,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) ATTN_STAMP(1);
+  volatile int* const fail_sm = reinterpret_cast<volatile int*>(smem + kOffFail);
 
   // Register split (warpgroup granularity, set at the top of each role's branch so the
   // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 64 +
-  // load/TMEM WG 64 = 65536 = 512 threads x 128 registers at launch.
+  // MMA issue / load / TMEM WG 64 = 65536 = 512 threads x 128 registers at launch.
   if (warp >= 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
   }
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      const uint64_t keep = l2_policy_evict_last();   // K/V: re-read by every CTA of the head
-      const uint64_t once = l2_policy_evict_first();  // Q: read once
-      // Q0, then K0, then Q1: the first QK needs only Q0 and K0.
-      auto load_q = [&](int q) {
-        const uint32_t bar = c.bar(kBarQFull + q);
-        const uint32_t dst = q_smem + q * kTileBytes;
-        mbar_arrive_expect_tx(bar, kTileBytes);
-        tma_load_4d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, hh, bb, once);
-        tma_load_4d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, hh, bb, once);
-      };
-      load_q(0);
+      const uint64_t keep = l2_policy_evict_last();  // K/V: re-read by every CTA of the head
       bool ok = true;
-      int issued = 0;
-      int s = 0;
-      for (int t = 0; t < 2 * n; ++t) {
+      int issued = 1;  // token 0 (K0) was loaded at set-up
+      for (int t = 1; t < 2 * n; ++t) {
         if (t >= kStages) {
           // The slot's previous token t-4 is free once Q tile 1's QK that follows its last
           // use has finished: K(j) after QK_1(j) (S_1(j) full), V(j) after PV_1(j), which
@@ -313,18 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ph = (prev & 1) ? (prev - 1) / 2 + 1 : prev / 2;
           if (!wait_bar(c, kBarSFull + 1, static_cast<uint32_t>(ph & 1), kRoleLoad)) { ok = false; break; }
         }
-        const uint32_t bar = c.bar(kBarKVFull + s);
-        const uint32_t dst = kv_smem + s * kTileBytes;
-        const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
-        const int row = (t >> 1) * kBlock;
-        if (!ATTN_WITHHELD(p, t)) {
-          mbar_arrive_expect_tx(bar, kTileBytes);
-          tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, keep);
-          tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, keep);
-        }
+        if (!ATTN_WITHHELD(p, t)) load_token(t, keep);
         issued = t + 1;
-        if (t == 0) load_q(1);
-        if (++s == kStages) s = 0;
       }
       if (!ok) {
         // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
@@ -335,33 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------------------------------ softmax (Q tile q)
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
-    const int q = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
-    const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
-    volatile int* const fail_sm = reinterpret_cast<volatile int*>(smem + kOffFail);
-    const float sl2 = p.scale_log2;
-    const int rem = p.S - (p.n_kv - 1) * kBlock;  // valid keys in the last tile, 1..128
-    float m_kept = -INFINITY;                 // kept row max, base-2 units
-    float l = 0.f;                            // running row sum that normalises O
-    float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
-    bool ok = true;
-
-    // The warpgroup's first thread issues this Q tile's MMAs: PV_q(i) as soon as the four
-    // warps have stored P_q(i) (a named barrier, no mbarrier round trip through another
-    // warp), then QK_q(i+1). The two leaders take turns, group by group (G_q(0) = QK_q(0),
-    // G_q(j) = PV_q(j-1) + QK_q(j)), in the order G0(0) G1(0) G0(1) G1(1) ...: one Q tile's
-    // softmax then runs while the tensor pipe works for the other (the pages' two-Q-tile
-    // ping-pong); without the turns both tiles drift into lockstep and the pipe idles while
-    // both softmaxes run. Turn barrier kBarTurn + q completes once per group the other
-    // leader has issued.
-    // The two leaders and the TMA producer sit on three different SM sub-partitions (warp w
-    // runs on sub-partition w % 4): a softmax warp that shares its sub-partition with the
-    // other Q tile's issuing thread or with the producer runs its exp loop measurably slower,
-    // and the warpgroup waits for its slowest warp.
-    const bool leader = (warp & 3) == q && lane == 0;
+  } else if (warp == kIssueWarp0 || warp == kIssueWarp1) {
+    // ------------------------------------------------------------------ MMA issue (Q tile q)
+    // One warp per Q tile issues that tile's MMAs from its first lane; the whole warp meets the
+    // tile's four softmax warps at one named barrier per part of P. In K/V tile i the group
+    // G_q(i+1) = PV_q(i) + QK_q(i+1) goes out part by part: the PV steps that read part k of
+    // P_q(i) right after the softmax has stored that part (early PV, the pages' Ch. 13), QK_q(i+1)
+    // after the last part, since it overwrites the columns P_q(i) occupies. The two warps take
+    // turns group by group (G0(0) G1(0) G0(1) G1(1) ...; the pages' two-Q-tile ping-pong):
+    // one tile's softmax then runs while the tensor pipe works for the other, and the pipe never
+    // interleaves the two tiles' accumulators MMA by MMA. Turn barrier kBarTurn + q completes
+    // once per group the other warp has issued.
+    const int q = warp == kIssueWarp1 ? 1 : 0;
     const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
     const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
     constexpr uint32_t kTileUnits = kTileBytes >> 4;            // one 32 KB tile, 16-byte units
@@ -374,75 +408,134 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dk = smem_desc_sw128(kv_smem, 16, 1024);
     const uint64_t dv = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
     // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
-    // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further).
-    auto issue_qk = [&](uint32_t k_slot) {
-      uint64_t a[8], b[8];
-      const uint64_t b0 = dk + k_slot * kTileUnits;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
-        a[kk] = dq + off;
-        b[kk] = b0 + off;
-      }
-      mma8_bf16_ss<0>(tSq, a, b, kIdescQK);
-    };
-    // The same, handing the turn to the other leader right after the eighth MMA, before the
-    // commit: the other leader sees the arrival a couple of hundred cycles later, so its
-    // first MMA follows without a gap in the tensor pipe, and every MMA of this group is
-    // queued ahead of the other leader's (the producer relies on that order, see below).
-    auto issue_qk_hand_over = [&](uint32_t k_slot) {
+    // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further). With
+    // hand_over, the turn passes to the other warp right after the eighth MMA, before the
+    // commit: the other warp sees the arrival a couple of hundred cycles later, so its first
+    // MMA follows without a gap in the tensor pipe, and every MMA of this group is queued ahead
+    // of the other warp's (the producer relies on that order).
+    auto issue_qk = [&](uint32_t k_slot, bool hand_over) {
       const uint64_t b0 = dk + k_slot * kTileUnits;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = ((kk >> 2) * kSliceBytes + (kk & 3) * 32) >> 4;
         mma_bf16_ss(tSq, dq + off, b0 + off, kIdescQK, kk > 0 ? 1u : 0u);
-        if (kk == 7) {
+        if (hand_over && kk == 7) {
           tc_fence_before();
           mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
         }
       }
     };
-    // O_q += P_q V: K16 step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16 per row) and
-    // V rows [16kk, 16kk+16) (2048 B further per step).
-    auto issue_pv = [&](uint32_t v_slot, bool first) {
-      uint32_t a[8];
-      uint64_t b[8];
+    // O_q += P_q V over K16 steps [k0, k1): step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16
+    // per row) and V rows [16kk, 16kk+16) (2048 B further per step).
+    auto issue_pv = [&](uint32_t v_slot, int k0, int k1, bool first) {
       const uint64_t b0 = dv + v_slot * kTileUnits;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        a[kk] = tSq + kk * 8;
-        b[kk] = b0 + kk * (2048 >> 4);
-      }
-      if (first) mma8_bf16_ts<0>(tOq, a, b, kIdescPV);
-      else mma8_bf16_ts<1>(tOq, a, b, kIdescPV);
+      for (int kk = 0; kk < 8; ++kk)
+        if (kk >= k0 && kk < k1)
+          mma_bf16_ts(tOq, tSq + kk * 8, b0 + kk * (2048 >> 4), kIdescPV, (first && kk == 0) ? 0u : 1u);
     };
     // K(i) is token 2i and V(i) token 2i+1 of the ring; token t sits in slot t % kStages
     // and its fill completes phase t / kStages of that slot's barrier.
     auto token_bar = [&](int t) { return kBarKVFull + t % kStages; };
     auto token_par = [&](int t) { return static_cast<uint32_t>((t / kStages) & 1); };
-    if (leader) {
-      ok = wait_bar(c, kBarQFull + q, 0, kRoleSoftmax) && wait_bar(c, token_bar(0), 0, kRoleSoftmax) &&
-           (q == 0 || wait_bar(c, kBarTurn + 1, 0, kRoleSoftmax));
+    bool ok = true;
+    if (lane == 0) {
+      ok = wait_bar(c, kBarQFull + q, 0, kRoleMma) && wait_bar(c, token_bar(0), 0, kRoleMma) &&
+           (q == 0 || wait_bar(c, kBarTurn + 1, 0, kRoleMma));
       if (ok) {
         tc_fence_after();
-        issue_qk(0);
+        issue_qk(0, false);
         mma_commit(c.bar(kBarSFull + q));
         tc_fence_before();
         mbar_arrive(c.bar(kBarTurn + (q ^ 1)));  // G_q(0) issued
       }
     }
-    // The warp-collective waits below need one value of ok in the whole warp.
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (int i = 0; i < n && ok; ++i) {
+      const int tv = 2 * i + 1, tk = 2 * i + 2;
+      const bool more = i + 1 < n;
+      // A softmax warp that gave up in the previous iteration recorded it before arriving at
+      // that iteration's barriers: stop before waiting for arrivals that will not come. (Its
+      // record is checked here rather than after each barrier, off the issue path; the MMAs
+      // issued in that iteration read stale P and are drained before TMEM is freed.)
+      if (fail_sm[q] != 0) {
+        ok = false;
+        break;
+      }
+      auto part = [&](auto pc) {
+        constexpr int pi = decltype(pc)::value;
+        constexpr int c0 = kPCut[pi], c1 = kPCut[pi + 1];
+        named_bar_sync(kBarP + 2 * pi + q, 160);  // pairs [c0, c1) of P_q(i) stored
+        if (ok && lane == 0) {
+          tc_fence_after();
+          if constexpr (pi == 0) {
+            // V(i), O_q safe for tile i (the correction warps' rescale, i >= 1) and this
+            // warp's turn for group G_q(i+1), probed together so their latencies overlap.
+            // Warp 0's turn for G0(i+1) follows G1(i) (phase i of its turn barrier); warp 1's
+            // for G1(i+1) follows G0(i+1) (phase i+1).
+            const uint32_t turn_par = static_cast<uint32_t>((q == 0 ? i : i + 1) & 1);
+            const uint32_t rdy = mbar_probe4(c.bar(token_bar(tv)), token_par(tv),
+                                             c.bar(kBarOSafe + q), static_cast<uint32_t>((i - 1) & 1),
+                                             c.bar(kBarTurn + q), turn_par,
+                                             c.bar(kBarTurn + q), turn_par);
+            ok = ((rdy & 1u) || wait_bar(c, token_bar(tv), token_par(tv), kRoleMma)) &&
+                 (i == 0 || (rdy & 2u) || wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleMma)) &&
+                 ((rdy & 4u) || wait_bar(c, kBarTurn + q, turn_par, kRoleMma));
+          }
+          if constexpr (pi == kPParts - 1) ok = ok && (!more || wait_bar(c, token_bar(tk), token_par(tk), kRoleMma));
+          if (ok) {
+            tc_fence_after();
+            issue_pv(static_cast<uint32_t>(tv % kStages), c0 / 8, c1 / 8, pi == 0 && i == 0);
+            if constexpr (pi == kPParts - 1) {
+              if (more) {
+                issue_qk(static_cast<uint32_t>(tk % kStages), true);  // hands the turn over
+                mma_commit(c.bar(kBarSFull + q));
+              } else {
+                mma_commit(c.bar(kBarOFull + q));
+                // Warp 0's last group still hands over; warp 1's has no successor.
+                if (q == 0) {
+                  tc_fence_before();
+                  mbar_arrive(c.bar(kBarTurn + 1));
+                }
+              }
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      };
+      static_for<kPParts>(part);
+    }
+    // Every MMA this warp issued must be complete before TMEM is freed: normally O_q full says
+    // so; otherwise a commit of everything issued so far does.
+    if (lane == 0) {
+      const bool fin = ok && wait_bar(c, kBarOFull + q, 0, kRoleMma);
+      if (!fin) {
+        mma_commit(c.bar(kBarMmaDone + q));
+        wait_slow(c, kBarMmaDone + q, 0, kRoleMma, false, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ softmax (Q tile q)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+    const int q = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
+    const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
+    const float sl2 = p.scale_log2;
+    const int rem = p.S - (p.n_kv - 1) * kBlock;  // valid keys in the last tile, 1..128
+    float m_kept = -INFINITY;                 // kept row max, base-2 units
+    float l = 0.f;                            // running row sum that normalises O
+    float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
+    bool ok = true;
 
     for (int i = 0; i < n; ++i) {
-      // S_q(i) full also means every earlier MMA of this Q tile, so PV_q(i-1) has read
-      // P_q(i-1). A warp whose leader gave up in the previous iteration waits no more.
-      if (!(ok && wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax))) {
-        // Give up: record the iteration for the other three warps, release them from this
-        // iteration's barrier and leave. They read the record after the barrier and leave at
-        // the same iteration, so no warp is ever left waiting there.
+      if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) {
+        // Give up: record the iteration for the issuing warp, release it from this
+        // iteration's barriers (it reads the record before the next ones) and leave.
         fail_sm[q] = i + 1;
-        named_bar_sync(2 + q, 128);
+        __threadfence_block();
+#pragma unroll
+        for (int pi = 0; pi < kPParts; ++pi) named_bar_arrive(kBarP + 2 * pi + q, 160);
         ok = false;
         break;
       }
@@ -496,8 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lb0 = 0.f, lb1 = 0.f, lb2 = 0.f, lb3 = 0.f;
       float lf0 = 0.f, lf1 = 0.f, lf2 = 0.f, lf3 = 0.f;
       uint32_t pk[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      auto pair = [&](int j) {
         float x0, x1;
         fma2(x0, x1, s[2 * j], s[2 * j + 1], sl2, sl2, neg_m, neg_m);
         const float p0 = ex2_ftz(x0);
@@ -514,62 +606,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j & 1) add2(lb2, lb3, lb2, lb3, b0, b1);
           else add2(lb0, lb1, lb0, lb1, b0, b1);
         }
-      }
+      };
+      // P_q(i) in parts: each part's BF16 pairs are stored into S_q's first columns, then the
+      // issuing warp is told (named barrier, no mbarrier round trip) so that the PV steps
+      // reading them start while the next part is computed.
+      auto part = [&](auto pc) {
+        constexpr int pi = decltype(pc)::value;
+        constexpr int c0 = kPCut[pi], c1 = kPCut[pi + 1];
+#pragma unroll
+        for (int j = c0; j < c1; ++j) pair(j);
+        tmem_st_cols<c0, c1>(tS, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_arrive(kBarP + 2 * pi + q, 160);
+      };
+      static_for<kPParts>(part);
       lf += (lf0 + lf1) + (lf2 + lf3);
       if constexpr (kRebase8) l += (lb0 + lb1) + (lb2 + lb3);
       else l = lf;
-      tmem_st32_x64(tS, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(2 + q, 128);  // P_q(i) stored by all four warps (or one gave up)
-      if (leader) {
-        tc_fence_after();
-        const int tv = 2 * i + 1, tk = 2 * i + 2;
-        const bool more = i + 1 < n;
-        // V(i), O_q safe for tile i (the correction warps' rescale, i >= 1), K(i+1) and this
-        // leader's turn for group G_q(i+1): the four probes are issued together so their
-        // latencies overlap. Leader 0's turn for G0(i+1) follows G1(i) (phase i of its turn
-        // barrier); leader 1's for G1(i+1) follows G0(i+1) (phase i+1).
-        const uint32_t turn_par = static_cast<uint32_t>((q == 0 ? i : i + 1) & 1);
-        const uint32_t rdy = mbar_probe4(c.bar(token_bar(tv)), token_par(tv),
-                                         c.bar(kBarOSafe + q), static_cast<uint32_t>((i - 1) & 1),
-                                         c.bar(token_bar(more ? tk : tv)), token_par(more ? tk : tv),
-                                         c.bar(kBarTurn + q), turn_par);
-        ok = ((rdy & 1u) || wait_bar(c, token_bar(tv), token_par(tv), kRoleSoftmax)) &&
-             (i == 0 || (rdy & 2u) || wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleSoftmax)) &&
-             (!more || (rdy & 4u) || wait_bar(c, token_bar(tk), token_par(tk), kRoleSoftmax)) &&
-             ((rdy & 8u) || wait_bar(c, kBarTurn + q, turn_par, kRoleSoftmax));
-        if (ok) {
-          tc_fence_after();
-          issue_pv(static_cast<uint32_t>(tv % kStages), i == 0);
-          if (more) {
-            issue_qk_hand_over(static_cast<uint32_t>(tk % kStages));  // hands the turn over
-            mma_commit(c.bar(kBarSFull + q));
-          } else {
-            mma_commit(c.bar(kBarOFull + q));
-            // Leader 0's last group still hands over; leader 1's has no successor.
-            if (q == 0) {
-              tc_fence_before();
-              mbar_arrive(c.bar(kBarTurn + 1));
-            }
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      // A record of i + 1 or less was written before this iteration's barrier by a warp that
-      // gave up; a later one (a warp already in the next iteration) is read again next time.
-      const int f = fail_sm[q];
-      if (f != 0 && f <= i + 1) { ok = false; break; }
     }
-    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the leader
-    // issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
+    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the issuing
+    // warp issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
     const bool fin = ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax);
     if ((warp & 3) == 0 && lane == 0) ATTN_STAMP(3 + q);
-    if (leader && !fin) {
-      // Give up: make sure every MMA this thread issued has finished before TMEM is freed.
-      mma_commit(c.bar(kBarMmaDone + q));
-      wait_slow(c, kBarMmaDone + q, 0, kRoleSoftmax, false, kDrainLimitNs);
-    }
     __syncwarp();
     // epilogue: O / l -> BF16 -> SW128 staging in the dead Q_q buffer -> one TMA store of
     // this warp's 32 rows (no cross-warp barrier; the two Q tiles finish independently).
@@ -647,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) ATTN_STAMP(5);
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kTmemWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

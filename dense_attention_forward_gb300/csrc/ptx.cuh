@@ -199,52 +199,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Eight K16 steps of one tile-sized MMA in a single asm block, every descriptor prepared by
-// the caller: nothing separates consecutive tcgen05.mma instructions, so the issuing thread
-// needs no issue slots between them (other warps' dense math competes for those slots).
-// kAcc0 is the accumulate flag of the first step; the other seven accumulate.
-template <int kAcc0>
-__device__ __forceinline__ void mma8_bf16_ss(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
-                                             uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t"
-      "setp.ne.b32 p0, %18, 0;\n\t"
-      "setp.eq.u32 p1, %17, %17;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, p1;\n}\n" ::"r"(d_tmem),
-      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
-      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
-      "r"(idesc), "n"(kAcc0)
-      : "memory");
-}
-
-template <int kAcc0>
-__device__ __forceinline__ void mma8_bf16_ts(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
-                                             uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t"
-      "setp.ne.b32 p0, %18, 0;\n\t"
-      "setp.eq.u32 p1, %17, %17;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, p1;\n}\n" ::"r"(d_tmem),
-      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
-      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
-      "r"(idesc), "n"(kAcc0)
-      : "memory");
-}
-
 // The two BF16 halves of `pk` as FP32 values, with byte permutes (integer ALU pipe).
 // On this part FMA-pipe instructions issued by other warps (scalar FFMA/FADD/FMUL, IMAD,
 // mixed-precision BF16 adds) slow the tensor pipe; byte permutes and the packed FP32x2
@@ -358,6 +312,34 @@ __device__ __forceinline__ void tmem_st32_x32(uint32_t taddr, const uint32_t (&r
 __device__ __forceinline__ void tmem_st32_x64(uint32_t taddr, const uint32_t (&r)[64]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n"
                :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32_x16(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                  "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                  "r"(r[7]) : "memory");
+}
+
+// Registers r[c0..c1) into columns [c0, c1) (multiples of 8) after taddr, with the widest
+// 32/16/8-column stores that fit.
+template <int c0, int c1>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[64]) {
+  if constexpr (c1 - c0 >= 32 && c0 % 32 == 0) {
+    tmem_st32_x32(taddr + c0, *reinterpret_cast<const uint32_t(*)[32]>(&r[c0]));
+    tmem_st_cols<c0 + 32, c1>(taddr, r);
+  } else if constexpr (c1 - c0 >= 16 && c0 % 16 == 0) {
+    tmem_st32_x16(taddr + c0, &r[c0]);
+    tmem_st_cols<c0 + 16, c1>(taddr, r);
+  } else if constexpr (c1 - c0 >= 8) {
+    tmem_st32_x8(taddr + c0, &r[c0]);
+    tmem_st_cols<c0 + 8, c1>(taddr, r);
+  }
 }
 
 // Waits for this thread's outstanding tcgen05.ld and ties the 128 destination registers to

@@ -182,8 +182,8 @@ const char* attn_status_string(int status);
  * ran attn_fwd. *word receives 0 when no wait gave up. Returns ATTN_OK, or
  * ATTN_ERR_UNSUPPORTED_DEVICE / ATTN_ERR_LAUNCH if the word could not be read.
  *
- * Word layout: 0xA77E0000 | role << 8 | barrier, role 1 = TMA producer, 3 = softmax / MMA
- * issue, 4 = O correction; barrier = the index of the mbarrier whose wait ran out.
+ * Word layout: 0xA77E0000 | role << 8 | barrier, role 1 = TMA producer, 2 = MMA issue,
+ * 3 = softmax, 4 = O correction; barrier = the index of the mbarrier whose wait ran out.
  */
 int attn_device_status(unsigned int* word, int reset);
 

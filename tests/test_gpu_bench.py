@@ -47,6 +47,7 @@ def test_bench_json_line():
     assert st["min"] <= st["median"] <= st["max"] and st["min"] <= st["mean"] <= st["max"]
     assert abs(st["mean"] - d["ms_per_step"]) < 1e-3
     assert d["value_best"] >= d["value_median"] > 0
+    assert abs(d["value_median"] - flops / (st["median"] * 1e-3) / 1e12) / d["value_median"] < 0.01
     e2e = d["e2e"]
     assert e2e["unit"] == "TFLOPS" and 0 < e2e["value"] < d["value"]
     assert e2e["device_status"] == 0 and e2e["outputs_equal_device_call"] is True
@@ -56,6 +57,20 @@ def test_bench_json_line():
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["unit"] == "TFLOPS" and cb["cores"] >= 1 and cb["value"] > 0
+
+
+def test_bench_main_roofline_is_the_main_workload_after_a_sweep():
+    # The sweep must not leak into the main line's roofline or median (a causal sweep entry
+    # last, as in the default sweep).
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5", "--warmup", "3",
+           "--workload", "tiny", "--sweep", "tiny", "--causal-sweep", "tiny", "--sweep-steps", "5",
+           "--e2e-steps", "3", "--no-cpu-baseline"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][-1])
+    assert abs(d["roofline"]["achieved"] - d["value"]) < 1e-6
+    flops = 4 * 1 * 1 * 256 * 256 * 128
+    assert abs(d["value_median"] - flops / (d["step_ms"]["median"] * 1e-3) / 1e12) / d["value_median"] < 0.01
 
 
 def test_bench_sweep_entries_carry_a_roofline():

@@ -22,7 +22,7 @@ from workloads import to_f64
 
 pytestmark = pytest.mark.gpu
 
-ROLES = {1: "TMA producer", 3: "softmax / MMA issue", 4: "O correction"}
+ROLES = {1: "TMA producer", 2: "MMA issue", 3: "softmax", 4: "O correction"}
 
 
 @pytest.fixture(scope="module")
