@@ -35,9 +35,9 @@ L2_FLUSH_BYTES = 256 << 20
 # keyed by sweep entry; each is valid only for the kernel source it was taken on (hash of the
 # kernel's CUDA sources), and is reported as null otherwise.
 TRAFFIC: dict[str, tuple[int, str]] = {
-    "s4k": (246420992, "63ed13ec744bee37"),         # 201,383,168 B read + 45,037,824 B written
-    "s16k": (245436928, "63ed13ec744bee37"),        # 201,375,744 B read + 44,061,184 B written
-    "s4k_causal": (244635904, "63ed13ec744bee37"),  # 201,544,960 B read + 43,090,944 B written
+    "s4k": (246832896, "eac846725b9afcdb"),         # 201,431,808 B read + 45,401,088 B written
+    "s16k": (248684288, "eac846725b9afcdb"),        # 201,376,000 B read + 47,308,288 B written
+    "s4k_causal": (245072896, "eac846725b9afcdb"),  # 201,548,032 B read + 43,524,864 B written
 }
 
 # Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64

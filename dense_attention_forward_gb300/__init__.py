@@ -32,7 +32,7 @@ def _check(name, t, shape=None):
 
 
 def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True,
-        stream=None, rebase_threshold: int = 0, causal: bool = False):
+        stream=None, rebase_threshold: int = 1, causal: bool = False):
     """Attention forward on the current CUDA stream (or `stream`).
 
     q, k, v: bfloat16 CUDA tensors shaped [B, H, S, 128] with a contiguous last dimension;
@@ -40,7 +40,8 @@ def fwd(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: boo
     to the kernel as they are. scale defaults to 1/sqrt(128).
     Returns (o, lse) with o bfloat16 [B, H, S, 128] (contiguous unless `out` is given) and
     lse float32 [B, H, S] (natural log), or (o, None) when return_lse is False.
-    rebase_threshold (0 or 8) selects the online-softmax rebase rule (see attn_fwd_ex).
+    rebase_threshold (1, the default of the C entry points, 0 or 8) selects the online-softmax
+    rebase rule (see attn_fwd_ex).
     causal=True applies the causal mask (query i sees keys j <= i; see attn_fwd_causal).
     """
     import torch

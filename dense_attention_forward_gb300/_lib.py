@@ -125,7 +125,7 @@ def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None
 
 def attn_fwd_ex(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None, B: int, H: int,
                 S: int, D: int, scale: float, rebase_threshold_log2: int, stream: int | None) -> int:
-    """Direct call of attn_fwd_ex (rebase threshold 0 or 8); returns the status code."""
+    """Direct call of attn_fwd_ex (rebase threshold 0, 1 or 8); returns the status code."""
     return lib().attn_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, S, D, scale,
                              rebase_threshold_log2, stream)
 

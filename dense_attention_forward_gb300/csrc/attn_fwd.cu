@@ -21,9 +21,9 @@
 //  * Softmax (Ch. 1 §B, Ch. 8, Ch. 11): 4 warps per Q tile, one thread per row, the whole
 //    128-score row in registers; base-2 exponent with scale*log2(e) folded into one factor,
 //    row max taken on raw scores; P is packed to BF16 pairs and stored over S in tensor
-//    memory. The kept row max follows the running max (rebase threshold 0), or, in the
-//    kRebase8 instantiation, moves only when a tile's max exceeds it by >= 8 (Ch. 11), with O
-//    then normalised by the sum of the BF16-rounded P. Only packed FP32x2 arithmetic, MUFU,
+//    memory. The kept row max moves only when a tile's max exceeds it by the rebase threshold
+//    (Ch. 11): 1 by default (P <= 2), 0 (the running max, P <= 1) or the pages' 8, with O then
+//    normalised by the sum of the BF16-rounded P. Only packed FP32x2 arithmetic, MUFU,
 //    conversions and byte permutes run per element: on this part scalar FP32 and IMAD work
 //    in other warps slows the tensor pipe.
 //  * Correction (Ch. 11, Ch. 12): 4 warps shared by both Q tiles rescale O in tensor memory
@@ -80,6 +80,7 @@ constexpr int kPParts = 3;
 constexpr int kPCut[kPParts + 1] = {0, 16, 40, 64};
 constexpr int kBarP = 2;  // named barrier of part k of Q tile q: kBarP + 2k + q (0 is __syncthreads)
 constexpr int kCausalGroup = 16;                 // causal launch order: heads per group
+constexpr int kDefaultRebase = 1;                // rebase threshold of attn_fwd, attn_fwd_causal, attn_fwd_host
 static_assert(kBarP + 2 * kPParts <= 16, "named barrier ids");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
@@ -234,16 +235,19 @@ __device__ __forceinline__ void static_for(F&& f) {
   }
 }
 
-// kRebase8: keep the row max until a tile's max exceeds it by 8 (base 2), the pages' Ch. 11
-// "skip O rescale"; P can then reach 2^8, and O is normalised by a second row sum over the
-// BF16-rounded P. Otherwise (threshold 0) the kept max is the running max, P <= 1 with the
-// row maximum exactly 1, and one fp32 row sum serves both O and lse.
+// kThr: the rebase threshold of the pages' Ch. 11 "skip O rescale", in base-2 units. The kept
+// row max moves (and O, l are rescaled) only when a tile's max exceeds it by kThr or more
+// (threshold 0: whenever it grows, so the kept max is the running max). P then stays below
+// 2^kThr. For 0 and 1 one fp32 row sum serves both O and lse: the BF16 rounding of P in the
+// PV product against the fp32 sum is at most 2^-9 relative per term, which for P <= 2 stays
+// well inside the output tolerance even on rows dominated by one key. For 8, P can reach 256
+// and O is normalised by a second row sum over the BF16-rounded P.
 // kCausal: query i sees keys j <= i (queries and keys share positions 0..S-1). The CTA of Q
 // tiles 2qp and 2qp+1 walks K/V tiles 0..2qp+1 only; its diagonal tiles are masked per
 // element, and Q tile 2qp runs tile 2qp+1 fully masked (P = 0) so both Q tiles keep the same
 // K/V schedule. CTAs are launched longest first (descending qp) inside groups of heads, which
 // shortens the tail of the grid and keeps each group's K/V in L2.
-template <bool kRebase8, bool kCausal>
+template <int kThr, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -572,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_kept = tile_max;
       } else {
         float alpha = 1.0f;
-        if (kRebase8 ? (tile_max - m_kept >= 8.0f) : (tile_max > m_kept)) {
+        if (kThr == 0 ? (tile_max > m_kept) : (tile_max - m_kept >= static_cast<float>(kThr))) {
           alpha = ex2_ftz(m_kept - tile_max);
-          if constexpr (kRebase8) l *= alpha;
+          if constexpr (kThr == 8) l *= alpha;
           lf *= alpha;
           m_kept = tile_max;
         }
@@ -600,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           add2(lf0, lf1, lf0, lf1, p0, p1);
         }
-        if constexpr (kRebase8) {
+        if constexpr (kThr == 8) {
           float b0, b1;
           bf16x2_to_f32x2(pk[j], b0, b1);
           if (j & 1) add2(lb2, lb3, lb2, lb3, b0, b1);
@@ -622,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       static_for<kPParts>(part);
       lf += (lf0 + lf1) + (lf2 + lf3);
-      if constexpr (kRebase8) l += (lb0 + lb1) + (lb2 + lb3);
+      if constexpr (kThr == 8) l += (lb0 + lb1) + (lb2 + lb3);
       else l = lf;
     }
     // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the issuing
@@ -763,14 +767,15 @@ int prepare_device(int* dev_out) {
     g_dev_state[dev].store(-1, std::memory_order_release);
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
-  if (cudaFuncSetAttribute(attn_fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess) {
+  auto smem_attr = [](const void* fn) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess;
+  };
+  if (!smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<0, false>)) ||
+      !smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<1, false>)) ||
+      !smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<8, false>)) ||
+      !smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<0, true>)) ||
+      !smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<1, true>)) ||
+      !smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<8, true>))) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
@@ -837,7 +842,8 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
                        const long long* vs, const long long* os, int rebase_threshold_log2,
                        int causal, int withhold, int check_only, void* stream) {
   using namespace gb300;
-  if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 8) return ATTN_ERR_INVALID_ARG;
+  if (rebase_threshold_log2 != 0 && rebase_threshold_log2 != 1 && rebase_threshold_log2 != 8)
+    return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (D != kHeadDim) return ATTN_ERR_UNSUPPORTED_DIM;
   if (!q || !k || !v || !o || !qs || !ks || !vs || !os) return ATTN_ERR_INVALID_ARG;
@@ -898,12 +904,16 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
 
   const dim3 grid(static_cast<unsigned>(BH * n_qp));
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  auto launch = [&](auto kernel) { kernel<<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm); };
   if (rebase_threshold_log2 == 8) {
-    if (causal) attn_fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
-    else attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+    if (causal) launch(attn_fwd_kernel<8, true>);
+    else launch(attn_fwd_kernel<8, false>);
+  } else if (rebase_threshold_log2 == 1) {
+    if (causal) launch(attn_fwd_kernel<1, true>);
+    else launch(attn_fwd_kernel<1, false>);
   } else {
-    if (causal) attn_fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
-    else attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm);
+    if (causal) launch(attn_fwd_kernel<0, true>);
+    else launch(attn_fwd_kernel<0, false>);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
@@ -928,7 +938,7 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
 int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                     int S, int D, float scale, void* stream) {
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 1, -1, 0, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, gb300::kDefaultRebase, 1, -1, 0, stream);
 }
 
 #ifdef ATTN_TEST_HOOKS
@@ -936,7 +946,7 @@ int attn_fwd_withhold(const void* q, const void* k, const void* v, void* o, floa
                       int S, int D, float scale, int token, void* stream) {
   if (token < 0) return ATTN_ERR_INVALID_ARG;
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
-  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, 0, 0, token, 0, stream);
+  return attn_launch(q, k, v, o, lse, B, H, S, D, scale, st, st, st, st, gb300::kDefaultRebase, 0, token, 0, stream);
 }
 #endif
 
@@ -947,7 +957,7 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
   if ((lse_h == nullptr) != (lse_d == nullptr)) return ATTN_ERR_INVALID_ARG;
   const long long st[3] = {static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
   // Everything the kernel launch would reject is rejected before any copy is enqueued.
-  int r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 2, stream);
+  int r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, gb300::kDefaultRebase, causal, -1, 2, stream);
   if (r != ATTN_OK) return r;
   const size_t bytes = static_cast<size_t>(B) * H * S * D * 2;
   const size_t lse_bytes = static_cast<size_t>(B) * H * S * 4;
@@ -956,7 +966,7 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
   if (gb300::overlaps(q_d, bytes, k_d, bytes) || gb300::overlaps(q_d, bytes, v_d, bytes) ||
       gb300::overlaps(k_d, bytes, v_d, bytes))
     return ATTN_ERR_INVALID_ARG;
-  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 1, stream);
+  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, gb300::kDefaultRebase, causal, -1, 1, stream);
   if (r != ATTN_OK) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(q_d, q_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
@@ -965,7 +975,7 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
-  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, 0, causal, -1, 0, stream);
+  r = attn_launch(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, scale, st, st, st, st, gb300::kDefaultRebase, causal, -1, 0, stream);
   if (r != ATTN_OK) return r;
   if (cudaMemcpyAsync(o_h, o_d, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       (lse_h && cudaMemcpyAsync(lse_h, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)) {
@@ -977,7 +987,7 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int S, int D, float scale, void* stream) {
-  return attn_fwd_ex(q, k, v, o, lse, B, H, S, D, scale, 0, stream);
+  return attn_fwd_ex(q, k, v, o, lse, B, H, S, D, scale, gb300::kDefaultRebase, stream);
 }
 
 const char* attn_status_string(int status) {

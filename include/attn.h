@@ -68,14 +68,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 /*
  * attn_fwd_ex -- attn_fwd with the online-softmax rebase threshold chosen by the caller
  * ("B200 attention kernel from scratch to ~SOTA in 60 figures (CUDA/PTX)", Ch. 11
- * "skip O rescale"). The result does not depend on it beyond rounding.
+ * "skip O rescale"): the kept row max, and with it the scaling of O and of the row sum, moves
+ * only when a K/V tile's max exceeds it by at least the threshold, in base-2 exponent units.
+ * The result does not depend on it beyond rounding.
  *
- *   rebase_threshold_log2 = 0 : the kept row max is the running max; P <= 1 (what attn_fwd
- *                               uses).
- *   rebase_threshold_log2 = 8 : the kept max moves only when a K/V tile's max exceeds it by
- *                               >= 8 in base-2 exponent units, as on the pages; P may reach
- *                               2^8 and the output is normalised by the sum of the
- *                               BF16-rounded P.
+ *   rebase_threshold_log2 = 1 : what attn_fwd, attn_fwd_causal and attn_fwd_host use; P <= 2,
+ *                               one fp32 row sum normalises O and gives lse.
+ *   rebase_threshold_log2 = 0 : the kept row max is the running max; P <= 1.
+ *   rebase_threshold_log2 = 8 : the pages' choice; P may reach 2^8 and the output is
+ *                               normalised by the sum of the BF16-rounded P.
  * Any other value: ATTN_ERR_INVALID_ARG. All other arguments, errors and ownership as attn_fwd.
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -13,7 +13,7 @@ extern "C" {
 #endif
 
 /*
- * attn_fwd_withhold -- runs attn_fwd (dense, rebase threshold 0) except that every CTA's TMA
+ * attn_fwd_withhold -- runs attn_fwd (dense, its default rebase threshold) except that every CTA's TMA
  * producer skips K/V token `token` (token 2i is K tile i, token 2i+1 is V tile i, tiles of 128
  * keys), so the waits that need it never complete. About two seconds after launch the first
  * such wait gives up and records its status word (see attn_device_status); every CTA then

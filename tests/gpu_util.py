@@ -12,8 +12,9 @@ O_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
 
 
-def run_gpu(q, k, v, scale, rebase_threshold=0, causal=False):
-    """q, k, v: CPU BF16 [B,H,S,D]. Returns (o, lse) as float64 numpy, via the C ABI."""
+def run_gpu(q, k, v, scale, rebase_threshold=1, causal=False):
+    """q, k, v: CPU BF16 [B,H,S,D]. Returns (o, lse) as float64 numpy, via the C ABI (rebase
+    threshold 1 is the library's default, the configuration the bench times)."""
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     o, lse = attn.fwd(qd, kd, vd, scale, rebase_threshold=rebase_threshold, causal=causal)
     torch.cuda.synchronize()
@@ -59,7 +60,7 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref):
     return stats
 
 
-def full_parity(q, k, v, scale, rebase_threshold=0, causal=False):
+def full_parity(q, k, v, scale, rebase_threshold=1, causal=False):
     o_gpu, lse_gpu = run_gpu(q, k, v, scale, rebase_threshold, causal)
     o_ref, lse_ref = ref.attention(to_f64(q), to_f64(k), to_f64(v), scale, causal=causal)
     return compare(o_gpu, lse_gpu, o_ref, lse_ref)

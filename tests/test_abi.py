@@ -112,7 +112,7 @@ def test_argument_errors_are_reported_before_any_cuda_call(lib, kw, expected):
     assert call(lib, **kw) == expected
 
 
-@pytest.mark.parametrize("thr,expected", [(1, 1), (-8, 1), (16, 1), (7, 1)])
+@pytest.mark.parametrize("thr,expected", [(2, 1), (-1, 1), (-8, 1), (16, 1), (7, 1)])
 def test_bad_rebase_threshold(lib, thr, expected):
     assert lib.attn_fwd_ex(Q, K, V, O, L, 1, 1, 256, 128, 0.088, thr, None) == expected
 

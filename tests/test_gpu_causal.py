@@ -14,7 +14,7 @@ from tests.gpu_util import compare, full_parity, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 @pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 256, 257, 383, 511, 512, 640, 1000])
 def test_causal_edge_lengths_full(S, thr):
     # Lengths around the 128-row tile and the 256-row CTA: diagonal tiles, the masked tile
@@ -23,7 +23,7 @@ def test_causal_edge_lengths_full(S, thr):
     full_parity(q, k, v, 1.0 / np.sqrt(128), thr, causal=True)
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 def test_causal_peaky_rows_full(thr):
     q, k, v = wl.make_custom(1, 2, 1500, seed=7, qk_gain=3.0)
     full_parity(q, k, v, 1.0 / np.sqrt(128), thr, causal=True)
@@ -38,7 +38,8 @@ def test_causal_first_row_is_exactly_v0():
     assert np.max(np.abs(lse[:, :, 0] - s00)) < 1e-4
 
 
-@pytest.mark.parametrize("name,thr", [("s4k", 0), ("s8k", 0), ("s16k", 0), ("ragged", 0), ("s16k", 8)])
+@pytest.mark.parametrize("name,thr", [("s4k", 1), ("s8k", 1), ("s16k", 1), ("ragged", 1), ("s4k", 0),
+                                      ("s16k", 8)])
 def test_causal_full_size_sampled(name, thr):
     w = wl.ALL[name]
     q, k, v = wl.make_qkv(w)

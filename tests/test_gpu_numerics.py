@@ -22,7 +22,7 @@ def test_tiny_scale_nearly_uniform():
     assert np.max(np.abs(o - to_f64(v).mean(axis=2, keepdims=True))) < 0.05
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 def test_large_scale_nearly_one_hot(thr):
     # Q, K x2 and scale 1: score spread ~45 per row, so almost every row is dominated by one key.
     q, k, v = wl.make_custom(1, 2, 600, seed=82, qk_gain=2.0)

@@ -18,14 +18,14 @@ def test_tiny_workload_full():
     full_parity(q, k, v, w.scale)
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 @pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 256, 257, 383, 640, 1000])
 def test_edge_lengths_full(S, thr):
     q, k, v = wl.make_custom(2, 3, S, seed=S)
     full_parity(q, k, v, 1.0 / np.sqrt(128), thr)
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 @pytest.mark.parametrize("S", [300, 1024, 1500])
 def test_peaky_rows_full(S, thr):
     # Q and K x3 before the BF16 cast: score std ~9, rows rebase often.
@@ -43,7 +43,7 @@ def test_rising_scores_rebase_every_tile():
     k = torch.randn(1, 2, S, 128, generator=g) * torch.linspace(0.2, 3.0, S).view(1, 1, S, 1)
     v = torch.randn(1, 2, S, 128, generator=g)
     q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
-    for thr in (0, 8):
+    for thr in (0, 1, 8):
         full_parity(q, k, v, 1.0 / np.sqrt(128), thr)
 
 
@@ -71,17 +71,18 @@ def test_other_scale():
 @pytest.mark.parametrize("name", ["s4k", "s8k", "s16k"])
 def test_full_size_workloads_every_row(name):
     # The three sequence lengths of the pages at their full sizes, in the launch configuration
-    # the bench times (threshold 0): every row of every head against the oracle (rows are
-    # independent, so the oracle runs them in blocks; about 0.55 / 1.1 / 2.2 TFLOP of fp64).
+    # the bench times (the default threshold 1): every row of every head against the oracle
+    # (rows are independent, so the oracle runs them in blocks; 0.55 / 1.1 / 2.2 TFLOP of fp64).
     w = wl.ALL[name]
     q, k, v = wl.make_qkv(w)
-    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale, 0)
+    o_gpu, lse_gpu = run_gpu(q, k, v, w.scale)
     o_ref, lse_ref = ref.attention(to_f64(q), to_f64(k), to_f64(v), w.scale, row_block=1024)
     stats = compare(o_gpu, lse_gpu, o_ref, lse_ref)
     assert stats["n_rows"] == w.B * w.H * w.S
 
 
-@pytest.mark.parametrize("name,thr", [("ragged", 0), ("s4k", 8), ("s16k", 8), ("ragged", 8)])
+@pytest.mark.parametrize("name,thr", [("ragged", 1), ("ragged", 0), ("s4k", 0), ("s4k", 8), ("s16k", 8),
+                                      ("ragged", 8)])
 def test_full_size_workloads_sampled(name, thr):
     w = wl.ALL[name]
     q, k, v = wl.make_qkv(w)
@@ -97,7 +98,7 @@ def test_full_size_workloads_sampled(name, thr):
     assert np.all(np.isfinite(lse_gpu))
 
 
-@pytest.mark.parametrize("thr", [0, 8])
+@pytest.mark.parametrize("thr", [0, 1, 8])
 def test_bshd_layout(thr):
     # [B, S, H, D] buffers viewed as [B, H, S, D] through transpose(1, 2): the kernel reads
     # and writes them in place through 4-D tensor maps.
