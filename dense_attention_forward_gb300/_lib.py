@@ -157,4 +157,6 @@ def check_device_status(reset: bool = True) -> None:
     word = device_status(reset)
     if word != 0:
         role = _ROLES.get((word >> 8) & 0xFF, "unknown role")
-        raise AttnError(6, f"kernel (status word {word:#010x}: {role}, mbarrier {word & 0xFF})")
+        idx = word & 0xFF
+        what = f"mbarrier {idx}" if idx < 18 else f"S-seen count of Q tile {idx - 18}"
+        raise AttnError(6, f"kernel (status word {word:#010x}: {role}, {what})")

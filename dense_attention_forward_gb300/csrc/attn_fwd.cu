@@ -4,9 +4,11 @@
 //
 // Design (after "B200 attention kernel from scratch to ~SOTA in 60 figures (CUDA/PTX)",
 // cited as [B200-attn]; its kernels were written for B200 and are prior art here):
-//  * Work split (Ch. 1 §ii, Ch. 5): one CTA owns two consecutive 128-row Q tiles of one
-//    (batch, head) and walks every 128-key K/V tile of that head; each K/V tile loaded into
-//    shared memory serves both Q tiles.
+//  * Work split (Ch. 1 §ii, Ch. 5): a work item is two consecutive 128-row Q tiles of one
+//    (batch, head), walked against every 128-key K/V tile of that head; each K/V tile loaded
+//    into shared memory serves both Q tiles. One CTA per SM walks a list of items (persistent
+//    grid), so the next item's Q loads and first QK overlap the current item's last tiles and
+//    epilogue instead of a CTA exit, launch and pipeline fill per item.
 //  * Loads (Ch. 3, Ch. 6): Q0, K0 and Q1 leave right after the barriers are initialised; one
 //    TMA warp then streams K and V as separate tokens through a kStages-slot ring of 32 KB
 //    SW128 slots; a slot is refilled once the second Q tile's S-full commit that follows its
@@ -32,15 +34,18 @@
 //    SW128 in the dead Q_q buffer and TMA-stores them (32-row boxes, no cross-warp barrier);
 //    lse = (m + log2 l) * ln 2 is written by the same threads.
 //
+// Barrier phases count across the items of a CTA: per K/V tile of the CTA's stream (S full,
+// O safe, the turns, the P parts), per item (Q full, O full) or per token (the K/V ring).
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
 // the first 64 columns of S_q. Warps 0-7 softmax, 8-11 correction, 12 and 13 MMA issue (13
 // also owns the TMEM allocation), 14 loads. Every mbarrier wait is bounded (about two
 // seconds); a CTA that gives up records the failure in a device status word, drains its own
 // TMA loads and MMAs, frees its tensor memory and exits. The only other barriers are the
 // CTA-wide ones at entry and exit, and the named barriers on which each Q tile's softmax warps
-// (arriving) meet its issuing warp (waiting), one per part of P: a softmax warp that gives up
-// records the iteration in shared memory and arrives at all of that iteration's barriers
-// before it leaves, and the issuing warp reads the record before it waits for the next ones.
+// (arriving) meet its issuing warp (waiting), one per part of P. Those have no timeout, so the
+// softmax warps only ever arrive for a tile whose S they have seen, and wait for a tile's S
+// until the issuing warp announces that it has stopped; the issuing warp only waits at a tile's
+// barriers after issuing that tile's QK (see wait_s_full).
 // The test-hook build (-DATTN_TEST_HOOKS, libattn_testhooks.so) adds attn_fwd_withhold, which
 // runs this path on purpose: its producer skips one K/V token, so the waits on that token run
 // out. The product build has neither that entry point nor the parameter.
@@ -79,30 +84,36 @@ constexpr int kTmemWarp = kIssueWarp1;
 constexpr int kPParts = 3;
 constexpr int kPCut[kPParts + 1] = {0, 16, 40, 64};
 constexpr int kBarP = 2;  // named barrier of part k of Q tile q: kBarP + 2k + q (0 is __syncthreads)
-constexpr int kCausalGroup = 16;                 // causal launch order: heads per group
 constexpr int kDefaultRebase = 1;                // rebase threshold of attn_fwd, attn_fwd_causal, attn_fwd_host
 static_assert(kBarP + 2 * kPParts <= 16, "named barrier ids");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // drain after a failure: 0.2 s
+// The softmax warps' wait for S, bounded well beyond the issuing warp's worst case (its waits
+// between two QK groups, each bounded by kWaitLimitNs; see wait_s_full).
+constexpr uint64_t kSWaitLimitNs = 10000000000ull;
 
 // Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;                                   // Q0, Q1 (later: O staging)
+constexpr int kOffQ = 0;                                   // Q0, Q1
 constexpr int kOffKV = kOffQ + 2 * kTileBytes;             // K/V ring
-constexpr int kOffBar = kOffKV + kStages * kTileBytes;     // mbarriers
+constexpr int kOffStage = kOffKV + kStages * kTileBytes;   // O staging: [2 tiles][4 warps] x 4 KB
+constexpr int kStageWarpBytes = 32 * 128;                  // 32 rows x 64 columns of BF16
+constexpr int kOffBar = kOffStage + 8 * kStageWarpBytes;   // mbarriers
 // barrier indices
 constexpr int kBarQFull = 0;                       // [2] Q_q landed (TMA bytes)
 constexpr int kBarKVFull = 2;                      // [kStages] token landed (TMA bytes)
-constexpr int kBarSFull = kBarKVFull + kStages;    // [2] S_q in TMEM (MMA commit); S_1 also frees K/V slots
+constexpr int kBarSFull = kBarKVFull + kStages;    // [2] S_q in TMEM (MMA commit)
 constexpr int kBarOSafe = kBarSFull + 2;           // [2] O_q rescaled or left as is (4 correction warps)
 constexpr int kBarOFull = kBarOSafe + 2;           // [2] last PV_q done (MMA commit)
 constexpr int kBarStats = kBarOFull + 2;           // [2] per-row rescale factors published (4 warps)
 constexpr int kBarMmaDone = kBarStats + 2;         // [2] drain after a failure (one per issuing warp)
 constexpr int kBarTurn = kBarMmaDone + 2;          // [2] MMA-group turn of Q tile q (from the other issuing warp)
 constexpr int kNumBars = kBarTurn + 2;
+constexpr int kSeenCode = kNumBars;                // status-word index of the wait on S-seen count q: kSeenCode + q
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kOffFail = kOffAbort + 4;                    // int[2]: iteration + 1 a softmax warp gave up
-constexpr int kOffAlpha = (kOffFail + 8 + 15) & ~15;       // float[2][128]
+constexpr int kOffFail = kOffAbort + 4;                    // int[2]: issuing warp q has stopped issuing
+constexpr int kOffSeen = kOffFail + 8;                     // int[2]: S_q tiles seen by the softmax warps
+constexpr int kOffAlpha = (kOffSeen + 8 + 15) & ~15;       // float[2][128]
 constexpr int kSmemUsed = kOffAlpha + 2 * kBlock * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for the 1024-byte alignment
 
@@ -150,8 +161,9 @@ struct Params {
   int S;            // sequence length
   int H;            // heads (the tensor maps are 4-D: {D, S, H, B})
   int n_kv;         // ceil(S / 128)
-  int n_qp;         // ceil(S / 256): CTAs per (b, h)
+  int n_qp;         // ceil(S / 256): Q-tile pairs per (b, h)
   int BH;           // B * H
+  int num_items;    // B * H * n_qp work items (a pair of Q tiles each)
   float scale_log2; // scale * log2(e)
 #ifdef ATTN_TEST_HOOKS
   int withhold;     // K/V token the producer never loads (bounded-wait test hook), -1: none
@@ -202,6 +214,66 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctl& c, int b, uint32_t pari
   return __all_sync(0xffffffffu, ok);
 }
 
+// The softmax warps' wait for S_q full (warp-uniform result). It does not give up on the CTA's
+// abort flag: it returns false only once the issuing warp has announced that it stopped issuing
+// (*stopped), or after kSWaitLimitNs. The issuing warp waits at a tile's named barriers only
+// after issuing that tile's QK, whose completion this wait always sees, so the softmax warps
+// never leave those barriers short of their arrivals, and they never arrive at a barrier twice
+// while the issuing warp has yet to pass it (a named barrier has no generations to tell the two
+// apart).
+__device__ __noinline__ bool wait_s_full_slow(uint32_t bar, uint32_t parity, volatile int* stopped,
+                                              volatile uint32_t* abort_flag, uint32_t code) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*stopped) return false;
+      if (global_timer_ns() - t0 > kSWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicCAS(&g_attn_status, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_s_full(const Ctl& c, int b, uint32_t parity, volatile int* stopped) {
+  bool ok = mbar_try_wait(c.bar(b), parity);
+  if (!ok)
+    ok = wait_s_full_slow(c.bar(b), parity, stopped, c.abort_flag,
+                          0xA77E0000u | (kRoleSoftmax << 8) | static_cast<uint32_t>(b));
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ int ld_acquire_shared(const volatile int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(const_cast<int*>(p))) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_shared(volatile int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(const_cast<int*>(p))), "r"(v) : "memory");
+}
+
+// The TMA producer's wait until *count >= target (a monotonic count, so unlike a parity wait it
+// cannot mistake a phase two steps ahead or behind for the one it wants); false if this CTA is
+// giving up.
+__device__ __noinline__ bool wait_count(const Ctl& c, const volatile int* count, int target, uint32_t code) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_shared(count) >= target) return true;
+    __nanosleep(32);
+    if ((it & 15u) == 0) {
+      if (*c.abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *c.abort_flag = 1u;
+        atomicCAS(&g_attn_status, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
 // One arrival per warp, after every lane's prior shared/tensor-memory writes are ordered by
 // __syncwarp (each lane has already fenced its tcgen05 stores where that matters).
 __device__ __forceinline__ void warp_arrive(const Ctl& c, int b, int lane) {
@@ -242,11 +314,11 @@ __device__ __forceinline__ void static_for(F&& f) {
 // PV product against the fp32 sum is at most 2^-9 relative per term, which for P <= 2 stays
 // well inside the output tolerance even on rows dominated by one key. For 8, P can reach 256
 // and O is normalised by a second row sum over the BF16-rounded P.
-// kCausal: query i sees keys j <= i (queries and keys share positions 0..S-1). The CTA of Q
+// kCausal: query i sees keys j <= i (queries and keys share positions 0..S-1). The item of Q
 // tiles 2qp and 2qp+1 walks K/V tiles 0..2qp+1 only; its diagonal tiles are masked per
 // element, and Q tile 2qp runs tile 2qp+1 fully masked (P = 0) so both Q tiles keep the same
-// K/V schedule. CTAs are launched longest first (descending qp) inside groups of heads, which
-// shortens the tail of the grid and keeps each group's K/V in L2.
+// K/V schedule. Items are dealt to the CTAs longest first in a snake order, which evens out
+// the CTAs' totals of K/V tiles.
 template <int kThr, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -257,28 +329,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw_addr);
 
-  // The warp index, broadcast from lane 0 so that the compiler knows it is warp-uniform: the
-  // role branches and every MMA descriptor derived from it then stay in uniform registers.
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
-  int qp, bh;
-  if constexpr (kCausal) {
-    // Heads in groups of kCausalGroup, longest CTA first inside each group: a group's K/V
-    // (16 heads x 2 MB at S = 4096) stays in L2 while its CTAs run, and the short CTAs of one
-    // group overlap the long ones of the next.
-    const int per_group = kCausalGroup * p.n_qp;
-    const int g = static_cast<int>(blockIdx.x) / per_group;
-    const int r = static_cast<int>(blockIdx.x) - g * per_group;
-    const int gh = min(kCausalGroup, p.BH - g * kCausalGroup);  // heads in this group
-    qp = p.n_qp - 1 - r / gh;
-    bh = g * kCausalGroup + r % gh;
-  } else {
-    qp = static_cast<int>(blockIdx.x) % p.n_qp;
-    bh = static_cast<int>(blockIdx.x) / p.n_qp;
-  }
-  const int hh = bh % p.H, bb = bh / p.H;
-  const int q0 = qp * 2 * kBlock;
-  const int n = kCausal ? min(p.n_kv, 2 * qp + 2) : p.n_kv;  // K/V tiles this CTA walks
+  // Work items are pairs of 128-row Q tiles of one (batch, head). CTA c takes the items of
+  // rounds r = 0, 1, ...: dense, item r * gridDim.x + c (items are numbered head-major, so the
+  // CTAs of one round share K/V in L2); causal, items sorted longest first across all heads and
+  // dealt out in a snake (c, then 2 * gridDim.x - 1 - c, ...) so that every CTA gets a similar
+  // total of K/V tiles.
+  const int item0 = static_cast<int>(blockIdx.x);
+  const int stride = static_cast<int>(gridDim.x);
+  auto item_of = [&](int r) {
+    return (kCausal && (r & 1)) ? r * stride + stride - 1 - item0 : r * stride + item0;
+  };
+  struct Item {
+    int qp, bh, hh, bb, q0, n;
+  };
+  auto item_at = [&](int it) {
+    Item r;
+    if constexpr (kCausal) {
+      r.qp = p.n_qp - 1 - it / p.BH;
+      r.bh = it % p.BH;
+    } else {
+      r.qp = it % p.n_qp;
+      r.bh = it / p.n_qp;
+    }
+    r.hh = r.bh % p.H;
+    r.bb = r.bh / p.H;
+    r.q0 = r.qp * 2 * kBlock;
+    r.n = kCausal ? min(p.n_kv, 2 * r.qp + 2) : p.n_kv;
+    return r;
+  };
 
   if (threadIdx.x == 0) {
     ATTN_STAMP(0);
@@ -292,23 +372,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_smem = base + kOffQ;
   const uint32_t kv_smem = base + kOffKV;
 
-  // Q tile q (two 64-column boxes) into its buffer, completion counted on its barrier.
-  auto load_q = [&](int q, uint64_t policy) {
+  auto load_q = [&](const Item& it, int q, uint64_t policy) {
     const uint32_t bar = c.bar(kBarQFull + q);
     const uint32_t dst = q_smem + q * kTileBytes;
     mbar_arrive_expect_tx(bar, kTileBytes);
-    tma_load_4d_hint(dst, &tm_q, bar, 0, q0 + q * kBlock, hh, bb, policy);
-    tma_load_4d_hint(dst + kSliceBytes, &tm_q, bar, 64, q0 + q * kBlock, hh, bb, policy);
+    tma_load_4d_hint(dst, &tm_q, bar, 0, it.q0 + q * kBlock, it.hh, it.bb, policy);
+    tma_load_4d_hint(dst + kSliceBytes, &tm_q, bar, 64, it.q0 + q * kBlock, it.hh, it.bb, policy);
   };
-  // K/V token t (K(t/2) for even t, V(t/2) for odd t) into ring slot t % kStages.
-  auto load_token = [&](int t, uint64_t policy) {
-    const uint32_t bar = c.bar(kBarKVFull + t % kStages);
-    const uint32_t dst = kv_smem + (t % kStages) * kTileBytes;
-    const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
-    const int row = (t >> 1) * kBlock;
+  // Global token T (K of the CTA's tile T/2 for even T, V for odd), local tile u/2 of item it.
+  auto load_token = [&](const Item& it, int T, int u, uint64_t policy) {
+    const uint32_t bar = c.bar(kBarKVFull + T % kStages);
+    const uint32_t dst = kv_smem + (T % kStages) * kTileBytes;
+    const CUtensorMap* map = (T & 1) ? &tm_v : &tm_k;
+    const int row = (u >> 1) * kBlock;
     mbar_arrive_expect_tx(bar, kTileBytes);
-    tma_load_4d_hint(dst, map, bar, 0, row, hh, bb, policy);
-    tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, hh, bb, policy);
+    tma_load_4d_hint(dst, map, bar, 0, row, it.hh, it.bb, policy);
+    tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, it.hh, it.bb, policy);
   };
 
   if (threadIdx.x == 0) {
@@ -328,16 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     *c.abort_flag = 0u;
     reinterpret_cast<volatile int*>(smem + kOffFail)[0] = 0;
     reinterpret_cast<volatile int*>(smem + kOffFail)[1] = 0;
+    reinterpret_cast<volatile int*>(smem + kOffSeen)[0] = 0;
+    reinterpret_cast<volatile int*>(smem + kOffSeen)[1] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
-    // The first loads (Q0, K0, then Q1: the first QK needs only Q0 and K0) leave before the
-    // TMEM allocation and the CTA-wide barrier; the producer continues with token 1.
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
-    const uint64_t once = l2_policy_evict_first();  // Q: read once
-    load_q(0, once);
-    if (!ATTN_WITHHELD(p, 0)) load_token(0, l2_policy_evict_last());
-    load_q(1, once);
+    const Item it = item_at(item_of(0));
+    const uint64_t once = l2_policy_evict_first();
+    load_q(it, 0, once);
+    if (!ATTN_WITHHELD(p, 0)) load_token(it, 0, 0, l2_policy_evict_last());
+    load_q(it, 1, once);
   }
   if (warp == kTmemWarp) {
     tmem_alloc(base + kOffTmemSlot, 512);
@@ -348,11 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) ATTN_STAMP(1);
-  volatile int* const fail_sm = reinterpret_cast<volatile int*>(smem + kOffFail);
+  volatile int* const issuer_stopped = reinterpret_cast<volatile int*>(smem + kOffFail);
+  // s_seen[q]: how many S_q tiles the softmax warps have seen complete (the CTA's global tile
+  // count). S_q(g) complete means QK_q(g) and every earlier MMA of Q tile q have finished, and
+  // the MMAs of Q tile 0 run ahead of those of Q tile 1 in the same tensor pipe.
+  volatile int* const s_seen = reinterpret_cast<volatile int*>(smem + kOffSeen);
 
-  // Register split (warpgroup granularity, set at the top of each role's branch so the
-  // compiler allocates each role within its share): 2 softmax WGs x 192 + correction 64 +
-  // MMA issue / load / TMEM WG 64 = 65536 = 512 threads x 128 registers at launch.
   if (warp >= 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
   }
@@ -361,27 +442,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      const uint64_t keep = l2_policy_evict_last();  // K/V: re-read by every CTA of the head
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t once = l2_policy_evict_first();
+      // Every wait is on the softmax warps' S-seen counts, which only grow. (A parity wait on the
+      // S barriers themselves could run two phases ahead of them at an item boundary, or find
+      // them two phases on, and take a wrong phase for the one it needs.)
+      const uint32_t code0 = 0xA77E0000u | (kRoleLoad << 8) | static_cast<uint32_t>(kSeenCode);
       bool ok = true;
-      int issued = 1;  // token 0 (K0) was loaded at set-up
-      for (int t = 1; t < 2 * n; ++t) {
-        if (t >= kStages) {
-          // The slot's previous token t-4 is free once Q tile 1's QK that follows its last
-          // use has finished: K(j) after QK_1(j) (S_1(j) full), V(j) after PV_1(j), which
-          // precedes QK_1(j+1) (S_1(j+1) full). The tensor pipe runs MMAs in issue order and
-          // Q tile 1's group starts after Q tile 0's, so both tiles' uses are done then.
-          // The producer is never more than one phase of S_1 behind (phase ph + 2 needs K(ph +
-          // 2), a later token), so the parity wait is unambiguous.
-          const int prev = t - kStages;
-          const int ph = (prev & 1) ? (prev - 1) / 2 + 1 : prev / 2;
-          if (!wait_bar(c, kBarSFull + 1, static_cast<uint32_t>(ph & 1), kRoleLoad)) { ok = false; break; }
+      int issued = 1;           // global token 0 (the first item's K0) was loaded at set-up
+      int gbase = 0;            // global index of the item's first K/V tile
+      int q_loads[2] = {1, 1};  // Q tile loads so far (the phases of the Q barriers)
+      for (int k = 0; item_of(k) < p.num_items && ok; ++k) {
+        const Item it = item_at(item_of(k));
+        for (int u = 0; u < 2 * it.n; ++u) {
+          const int T = 2 * gbase + u;
+          if (T == 0) continue;
+          if (k > 0 && u == 0) {
+            // Q_0 of this item replaces the previous item's once QK_0 of its last tile is done.
+            if (!wait_count(c, s_seen + 0, gbase, code0)) { ok = false; break; }
+            load_q(it, 0, once);
+            ++q_loads[0];
+          }
+          if (T >= kStages) {
+            // The slot's previous token: K of tile g is free once QK_1(g) is done, V of tile g
+            // once QK_1(g + 1) is (its commit covers PV_1(g)); Q tile 0's MMAs run first.
+            const int prev = T - kStages;
+            if (!wait_count(c, s_seen + 1, prev / 2 + 1 + (prev & 1), code0 + 1)) { ok = false; break; }
+          }
+          if (!ATTN_WITHHELD(p, T)) load_token(it, T, u, keep);
+          issued = T + 1;
+          if (k > 0 && u == 0) {
+            if (!wait_count(c, s_seen + 1, gbase, code0 + 1)) { ok = false; break; }
+            load_q(it, 1, once);
+            ++q_loads[1];
+          }
         }
-        if (!ATTN_WITHHELD(p, t)) load_token(t, keep);
-        issued = t + 1;
+        gbase += it.n;
       }
       if (!ok) {
-        // Give up: wait (bounded, ignoring the abort flag) for loads that may be in flight.
-        for (int q = 0; q < 2; ++q) wait_slow(c, kBarQFull + q, 0, kRoleLoad, false, kDrainLimitNs);
+        // Drain: the last load of each Q tile and of the ring slots still owed.
+        for (int q = 0; q < 2; ++q)
+          wait_slow(c, kBarQFull + q, static_cast<uint32_t>((q_loads[q] - 1) & 1), kRoleLoad, false, kDrainLimitNs);
         for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
           if (!ATTN_WITHHELD(p, t))
             wait_slow(c, kBarKVFull + t % kStages, (t / kStages) & 1, kRoleLoad, false, kDrainLimitNs);
@@ -390,33 +491,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kIssueWarp0 || warp == kIssueWarp1) {
     // ------------------------------------------------------------------ MMA issue (Q tile q)
-    // One warp per Q tile issues that tile's MMAs from its first lane; the whole warp meets the
-    // tile's four softmax warps at one named barrier per part of P. In K/V tile i the group
-    // G_q(i+1) = PV_q(i) + QK_q(i+1) goes out part by part: the PV steps that read part k of
-    // P_q(i) right after the softmax has stored that part (early PV, the pages' Ch. 13), QK_q(i+1)
-    // after the last part, since it overwrites the columns P_q(i) occupies. The two warps take
-    // turns group by group (G0(0) G1(0) G0(1) G1(1) ...; the pages' two-Q-tile ping-pong):
-    // one tile's softmax then runs while the tensor pipe works for the other, and the pipe never
-    // interleaves the two tiles' accumulators MMA by MMA. Turn barrier kBarTurn + q completes
-    // once per group the other warp has issued.
     const int q = warp == kIssueWarp1 ? 1 : 0;
-    const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-    const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
-    constexpr uint32_t kTileUnits = kTileBytes >> 4;            // one 32 KB tile, 16-byte units
+    const uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+    const uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
+    constexpr uint32_t kTileUnits = kTileBytes >> 4;
     const uint32_t tSq = tmem + q * 128u, tOq = tmem + 256u + q * 128u;
-    // Descriptors: K-major SW128 (Q, K): 8-row atoms 1024 B apart (SBO), LBO unused.
-    // MN-major SW128 (V): 8-row groups along K 1024 B apart (SBO), the two 64-wide halves
-    // of N 16 KB apart (LBO). The start-address field (bits 0-13, 16-byte units) is moved by
-    // plain 64-bit addition; it never carries out of its field (addresses < 256 KB).
     const uint64_t dq = smem_desc_sw128(q_smem + q * kTileBytes, 16, 1024);
     const uint64_t dk = smem_desc_sw128(kv_smem, 16, 1024);
     const uint64_t dv = smem_desc_sw128(kv_smem, kSliceBytes, 1024);
-    // S_q = Q_q K^T: 8 K16 steps; steps 0-3 read the first 64-column slice (32 B apart
-    // inside the 128-B swizzle row), steps 4-7 the second slice (16 KB further). With
-    // hand_over, the turn passes to the other warp right after the eighth MMA, before the
-    // commit: the other warp sees the arrival a couple of hundred cycles later, so its first
-    // MMA follows without a gap in the tensor pipe, and every MMA of this group is queued ahead
-    // of the other warp's (the producer relies on that order).
     auto issue_qk = [&](uint32_t k_slot, bool hand_over) {
       const uint64_t b0 = dk + k_slot * kTileUnits;
 #pragma unroll
@@ -429,8 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    // O_q += P_q V over K16 steps [k0, k1): step kk takes P columns [8kk, 8kk+8) of S_q (16 BF16
-    // per row) and V rows [16kk, 16kk+16) (2048 B further per step).
     auto issue_pv = [&](uint32_t v_slot, int k0, int k1, bool first) {
       const uint64_t b0 = dv + v_slot * kTileUnits;
 #pragma unroll
@@ -438,8 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kk >= k0 && kk < k1)
           mma_bf16_ts(tOq, tSq + kk * 8, b0 + kk * (2048 >> 4), kIdescPV, (first && kk == 0) ? 0u : 1u);
     };
-    // K(i) is token 2i and V(i) token 2i+1 of the ring; token t sits in slot t % kStages
-    // and its fill completes phase t / kStages of that slot's barrier.
     auto token_bar = [&](int t) { return kBarKVFull + t % kStages; };
     auto token_par = [&](int t) { return static_cast<uint32_t>((t / kStages) & 1); };
     bool ok = true;
@@ -451,39 +529,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(0, false);
         mma_commit(c.bar(kBarSFull + q));
         tc_fence_before();
-        mbar_arrive(c.bar(kBarTurn + (q ^ 1)));  // G_q(0) issued
+        mbar_arrive(c.bar(kBarTurn + (q ^ 1)));
       }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    for (int i = 0; i < n && ok; ++i) {
-      const int tv = 2 * i + 1, tk = 2 * i + 2;
+    // One flat loop over the CTA's stream of K/V tiles: gt counts tiles across items, i is the
+    // tile within the current item, n its tile count.
+    int k = 0;
+    int n = kCausal ? item_at(item_of(0)).n : p.n_kv;
+    bool next_item = item_of(1) < p.num_items;
+    for (int gt = 0, i = 0; ok; ++gt) {
+      const int tv = 2 * gt + 1, tk = 2 * gt + 2;
       const bool more = i + 1 < n;
-      // A softmax warp that gave up in the previous iteration recorded it before arriving at
-      // that iteration's barriers: stop before waiting for arrivals that will not come. (Its
-      // record is checked here rather than after each barrier, off the issue path; the MMAs
-      // issued in that iteration read stale P and are drained before TMEM is freed.)
-      if (fail_sm[q] != 0) {
-        ok = false;
-        break;
-      }
       auto part = [&](auto pc) {
         constexpr int pi = decltype(pc)::value;
         constexpr int c0 = kPCut[pi], c1 = kPCut[pi + 1];
-        named_bar_sync(kBarP + 2 * pi + q, 160);  // pairs [c0, c1) of P_q(i) stored
+        named_bar_sync(kBarP + 2 * pi + q, 160);
         if (ok && lane == 0) {
           tc_fence_after();
           if constexpr (pi == 0) {
-            // V(i), O_q safe for tile i (the correction warps' rescale, i >= 1) and this
-            // warp's turn for group G_q(i+1), probed together so their latencies overlap.
-            // Warp 0's turn for G0(i+1) follows G1(i) (phase i of its turn barrier); warp 1's
-            // for G1(i+1) follows G0(i+1) (phase i+1).
-            const uint32_t turn_par = static_cast<uint32_t>((q == 0 ? i : i + 1) & 1);
+            const uint32_t turn_par = static_cast<uint32_t>((q == 0 ? gt : gt + 1) & 1);
             const uint32_t rdy = mbar_probe4(c.bar(token_bar(tv)), token_par(tv),
-                                             c.bar(kBarOSafe + q), static_cast<uint32_t>((i - 1) & 1),
+                                             c.bar(kBarOSafe + q), static_cast<uint32_t>((gt - 1) & 1),
                                              c.bar(kBarTurn + q), turn_par,
                                              c.bar(kBarTurn + q), turn_par);
             ok = ((rdy & 1u) || wait_bar(c, token_bar(tv), token_par(tv), kRoleMma)) &&
-                 (i == 0 || (rdy & 2u) || wait_bar(c, kBarOSafe + q, (i - 1) & 1, kRoleMma)) &&
+                 (gt == 0 || (rdy & 2u) || wait_bar(c, kBarOSafe + q, (gt - 1) & 1, kRoleMma)) &&
                  ((rdy & 4u) || wait_bar(c, kBarTurn + q, turn_par, kRoleMma));
           }
           if constexpr (pi == kPParts - 1) ok = ok && (!more || wait_bar(c, token_bar(tk), token_par(tk), kRoleMma));
@@ -492,12 +563,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv(static_cast<uint32_t>(tv % kStages), c0 / 8, c1 / 8, pi == 0 && i == 0);
             if constexpr (pi == kPParts - 1) {
               if (more) {
-                issue_qk(static_cast<uint32_t>(tk % kStages), true);  // hands the turn over
+                issue_qk(static_cast<uint32_t>(tk % kStages), true);
                 mma_commit(c.bar(kBarSFull + q));
               } else {
                 mma_commit(c.bar(kBarOFull + q));
-                // Warp 0's last group still hands over; warp 1's has no successor.
-                if (q == 0) {
+                if (next_item) {
+                  ok = wait_bar(c, token_bar(tk), token_par(tk), kRoleMma) &&
+                       wait_bar(c, kBarQFull + q, static_cast<uint32_t>((k + 1) & 1), kRoleMma);
+                  if (ok) {
+                    tc_fence_after();
+                    issue_qk(static_cast<uint32_t>(tk % kStages), true);
+                    mma_commit(c.bar(kBarSFull + q));
+                  }
+                } else if (q == 0) {
                   tc_fence_before();
                   mbar_arrive(c.bar(kBarTurn + 1));
                 }
@@ -508,11 +586,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       };
       static_for<kPParts>(part);
+      if (more) {
+        ++i;
+      } else {
+        ++k;
+        if (!next_item) break;
+        i = 0;
+        n = kCausal ? item_at(item_of(k)).n : p.n_kv;
+        next_item = item_of(k + 1) < p.num_items;
+      }
     }
-    // Every MMA this warp issued must be complete before TMEM is freed: normally O_q full says
-    // so; otherwise a commit of everything issued so far does.
+    if (!ok && lane == 0) {
+      // No further QK for this tile: the softmax warps waiting for one may leave.
+      issuer_stopped[q] = 1;
+      __threadfence_block();
+    }
     if (lane == 0) {
-      const bool fin = ok && wait_bar(c, kBarOFull + q, 0, kRoleMma);
+      const bool fin = ok && wait_bar(c, kBarOFull + q, static_cast<uint32_t>((k - 1) & 1), kRoleMma);
       if (!fin) {
         mma_commit(c.bar(kBarMmaDone + q));
         wait_slow(c, kBarMmaDone + q, 0, kRoleMma, false, kDrainLimitNs);
@@ -523,152 +613,156 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ softmax (Q tile q)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
     const int q = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;  // row inside the Q tile = TMEM lane
+    const int row = (warp & 3) * 32 + lane;
     const uint32_t tS = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * 128u;
     const float sl2 = p.scale_log2;
-    const int rem = p.S - (p.n_kv - 1) * kBlock;  // valid keys in the last tile, 1..128
-    float m_kept = -INFINITY;                 // kept row max, base-2 units
-    float l = 0.f;                            // running row sum that normalises O
-    float lf = 0.f;                           // running row sum of fp32 P (logsumexp)
+    const int rem = p.S - (p.n_kv - 1) * kBlock;
+    const uint32_t stage = base + kOffStage + (q * 4 + (warp & 3)) * kStageWarpBytes;
     bool ok = true;
-
-    for (int i = 0; i < n; ++i) {
-      if (!wait_bar_warp(c, kBarSFull + q, i & 1, kRoleSoftmax)) {
-        // Give up: record the iteration for the issuing warp, release it from this
-        // iteration's barriers (it reads the record before the next ones) and leave.
-        fail_sm[q] = i + 1;
-        __threadfence_block();
+    int gbase = 0, k = 0;
+    for (; item_of(k) < p.num_items && ok; ++k) {
+      const Item it = item_at(item_of(k));
+      const bool next_item = item_of(k + 1) < p.num_items;
+      float m_kept = -INFINITY;
+      float l = 0.f;
+      float lf = 0.f;
+      for (int i = 0; i < it.n; ++i) {
+        const int gt = gbase + i;
+        if (!wait_s_full(c, kBarSFull + q, gt & 1, issuer_stopped + q)) {
+          ok = false;  // no QK_q(gt) is coming: leave without arriving at its barriers
+          break;
+        }
+        if ((warp & 3) == 0 && lane == 0) st_release_shared(s_seen + q, gt + 1);
+        if (gt == 0 && warp == 0 && lane == 0) ATTN_STAMP(2);
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32_x128_sync(tS, sr);
+        float s[128];
 #pragma unroll
-        for (int pi = 0; pi < kPParts; ++pi) named_bar_arrive(kBarP + 2 * pi + q, 160);
+        for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sr[j]);
+        if (i == p.n_kv - 1 && rem < kBlock) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) s[j] = (j < rem) ? s[j] : -INFINITY;
+        }
+        if (kCausal && i >= 2 * it.qp + q) {
+          const int lim = it.q0 + q * kBlock + row - i * kBlock;
+#pragma unroll
+          for (int j = 0; j < 128; ++j) s[j] = (j <= lim) ? s[j] : -INFINITY;
+        }
+        float mx[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx[j] = fmaxf(s[2 * j], s[2 * j + 1]);
+#pragma unroll
+        for (int j = 8; j < 128; j += 8) {
+          mx[0] = max3(mx[0], s[j + 0], s[j + 1]);
+          mx[1] = max3(mx[1], s[j + 2], s[j + 3]);
+          mx[2] = max3(mx[2], s[j + 4], s[j + 5]);
+          mx[3] = max3(mx[3], s[j + 6], s[j + 7]);
+        }
+        const float tile_max = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
+        if (i == 0) {
+          m_kept = tile_max;
+        } else {
+          float alpha = 1.0f;
+          if (kThr == 0 ? (tile_max > m_kept) : (tile_max - m_kept >= static_cast<float>(kThr))) {
+            alpha = ex2_ftz(m_kept - tile_max);
+            if constexpr (kThr == 8) l *= alpha;
+            lf *= alpha;
+            m_kept = tile_max;
+          }
+          alpha_sm[q * kBlock + row] = alpha;
+          warp_arrive(c, kBarStats + q, lane);
+        }
+        const float neg_m = -m_kept;
+        float lb0 = 0.f, lb1 = 0.f, lb2 = 0.f, lb3 = 0.f;
+        float lf0 = 0.f, lf1 = 0.f, lf2 = 0.f, lf3 = 0.f;
+        uint32_t pk[64];
+        auto pair = [&](int j) {
+          float x0, x1;
+          fma2(x0, x1, s[2 * j], s[2 * j + 1], sl2, sl2, neg_m, neg_m);
+          const float p0 = ex2_ftz(x0);
+          const float p1 = ex2_ftz(x1);
+          pk[j] = pack_bf16x2(p0, p1);
+          if (j & 1) {
+            add2(lf2, lf3, lf2, lf3, p0, p1);
+          } else {
+            add2(lf0, lf1, lf0, lf1, p0, p1);
+          }
+          if constexpr (kThr == 8) {
+            float b0, b1;
+            bf16x2_to_f32x2(pk[j], b0, b1);
+            if (j & 1) add2(lb2, lb3, lb2, lb3, b0, b1);
+            else add2(lb0, lb1, lb0, lb1, b0, b1);
+          }
+        };
+        auto part = [&](auto pc) {
+          constexpr int pi = decltype(pc)::value;
+          constexpr int c0 = kPCut[pi], c1 = kPCut[pi + 1];
+#pragma unroll
+          for (int j = c0; j < c1; ++j) pair(j);
+          tmem_st_cols<c0, c1>(tS, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          named_bar_arrive(kBarP + 2 * pi + q, 160);
+        };
+        static_for<kPParts>(part);
+        lf += (lf0 + lf1) + (lf2 + lf3);
+        if constexpr (kThr == 8) l += (lb0 + lb1) + (lb2 + lb3);
+        else l = lf;
+      }
+      if (!ok) break;
+      const bool fin = wait_bar_warp(c, kBarOFull + q, static_cast<uint32_t>(k & 1), kRoleSoftmax);
+      if (k == 0 && (warp & 3) == 0 && lane == 0) ATTN_STAMP(3 + q);
+      if (!fin) {
         ok = false;
         break;
       }
-      if (i == 0 && warp == 0 && lane == 0) ATTN_STAMP(2);
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld32_x128_sync(tS, sr);
-      float s[128];
-#pragma unroll
-      for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sr[j]);
-      if (i == p.n_kv - 1 && rem < kBlock) {
-#pragma unroll
-        for (int j = 0; j < 128; ++j) s[j] = (j < rem) ? s[j] : -INFINITY;
-      }
-      if (kCausal && i >= 2 * qp + q) {
-        // Diagonal tile (and, for Q tile 2qp, the tile after it): column j is key
-        // i*128 + j, visible to this row while it is <= the row's position.
-        const int lim = q0 + q * kBlock + row - i * kBlock;
-#pragma unroll
-        for (int j = 0; j < 128; ++j) s[j] = (j <= lim) ? s[j] : -INFINITY;
-      }
-      float mx[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mx[j] = fmaxf(s[2 * j], s[2 * j + 1]);
-#pragma unroll
-      for (int j = 8; j < 128; j += 8) {
-        mx[0] = max3(mx[0], s[j + 0], s[j + 1]);
-        mx[1] = max3(mx[1], s[j + 2], s[j + 3]);
-        mx[2] = max3(mx[2], s[j + 4], s[j + 5]);
-        mx[3] = max3(mx[3], s[j + 6], s[j + 7]);
-      }
-      const float tile_max = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
-      if (i == 0) {
-        m_kept = tile_max;
-      } else {
-        float alpha = 1.0f;
-        if (kThr == 0 ? (tile_max > m_kept) : (tile_max - m_kept >= static_cast<float>(kThr))) {
-          alpha = ex2_ftz(m_kept - tile_max);
-          if constexpr (kThr == 8) l *= alpha;
-          lf *= alpha;
-          m_kept = tile_max;
-        }
-        alpha_sm[q * kBlock + row] = alpha;
-        warp_arrive(c, kBarStats + q, lane);
-      }
-      const float neg_m = -m_kept;
-      // lf adds the fp32 P (for the logsumexp, and for O at threshold 0). At threshold 8, lb
-      // adds the BF16-rounded P that the PV product consumes and normalises O: numerator and
-      // denominator then carry the same weights (P reaches 256 there, and a fp32-vs-BF16
-      // mismatch would show on rows dominated by one key).
-      float lb0 = 0.f, lb1 = 0.f, lb2 = 0.f, lb3 = 0.f;
-      float lf0 = 0.f, lf1 = 0.f, lf2 = 0.f, lf3 = 0.f;
-      uint32_t pk[64];
-      auto pair = [&](int j) {
-        float x0, x1;
-        fma2(x0, x1, s[2 * j], s[2 * j + 1], sl2, sl2, neg_m, neg_m);
-        const float p0 = ex2_ftz(x0);
-        const float p1 = ex2_ftz(x1);
-        pk[j] = pack_bf16x2(p0, p1);
-        if (j & 1) {
-          add2(lf2, lf3, lf2, lf3, p0, p1);
-        } else {
-          add2(lf0, lf1, lf0, lf1, p0, p1);
-        }
-        if constexpr (kThr == 8) {
-          float b0, b1;
-          bf16x2_to_f32x2(pk[j], b0, b1);
-          if (j & 1) add2(lb2, lb3, lb2, lb3, b0, b1);
-          else add2(lb0, lb1, lb0, lb1, b0, b1);
-        }
-      };
-      // P_q(i) in parts: each part's BF16 pairs are stored into S_q's first columns, then the
-      // issuing warp is told (named barrier, no mbarrier round trip) so that the PV steps
-      // reading them start while the next part is computed.
-      auto part = [&](auto pc) {
-        constexpr int pi = decltype(pc)::value;
-        constexpr int c0 = kPCut[pi], c1 = kPCut[pi + 1];
-#pragma unroll
-        for (int j = c0; j < c1; ++j) pair(j);
-        tmem_st_cols<c0, c1>(tS, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_arrive(kBarP + 2 * pi + q, 160);
-      };
-      static_for<kPParts>(part);
-      lf += (lf0 + lf1) + (lf2 + lf3);
-      if constexpr (kThr == 8) l += (lb0 + lb1) + (lb2 + lb3);
-      else l = lf;
-    }
-    // O_q full: PV_q(n-1) done, after the correction warps' last rescale of O_q (the issuing
-    // warp issued it after their O-safe arrival) and after QK_q(n-1), Q_q's last reader.
-    const bool fin = ok && wait_bar_warp(c, kBarOFull + q, 0, kRoleSoftmax);
-    if ((warp & 3) == 0 && lane == 0) ATTN_STAMP(3 + q);
-    __syncwarp();
-    // epilogue: O / l -> BF16 -> SW128 staging in the dead Q_q buffer -> one TMA store of
-    // this warp's 32 rows (no cross-warp barrier; the two Q tiles finish independently).
-    if (fin) {
+      // epilogue: O / l -> BF16 -> this warp's 4 KB staging (32 rows x 64 columns, SW128) ->
+      // TMA store, twice (columns 0-63, 64-127). O_q is released to the next item's first PV as
+      // soon as it has been read out of tensor memory.
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256u + q * 128u;
       uint32_t o[128];
       tmem_ld32_x128_sync(tO, o);
-      const uint32_t stage = q_smem + q * kTileBytes;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunk ch = columns 8ch..8ch+7
-        uint32_t w4[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          w4[t] = pack_bf16x2(__uint_as_float(o[8 * ch + 2 * t]) * inv_l,
-                              __uint_as_float(o[8 * ch + 2 * t + 1]) * inv_l);
-        const uint32_t addr = stage + (ch >> 3) * kSliceBytes + row * 128 +
-                              (static_cast<uint32_t>((ch & 7) ^ (row & 7)) << 4);
-        st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
+      if (next_item) {
+        tc_fence_before();
+        warp_arrive(c, kBarOSafe + q, lane);  // O_q drained
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      const int r0 = q0 + q * kBlock + (warp & 3) * 32;
-      if (lane == 0 && r0 < p.S) {
-        const uint32_t wst = stage + (warp & 3) * 32 * 128;
-        tma_store_4d(&tm_o, wst, 0, r0, hh, bb);
-        tma_store_4d(&tm_o, wst + kSliceBytes, 64, r0, hh, bb);
-        tma_store_commit();
-        tma_store_wait_read_all();
+      const int r0 = it.q0 + q * kBlock + (warp & 3) * 32;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1 || k > 0) {
+          // the previous store out of this staging has been read
+          if (lane == 0) tma_store_wait_read_all();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int cc = half * 8 + ch;
+          uint32_t w4[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            w4[t] = pack_bf16x2(__uint_as_float(o[8 * cc + 2 * t]) * inv_l,
+                                __uint_as_float(o[8 * cc + 2 * t + 1]) * inv_l);
+          const uint32_t addr = stage + lane * 128 + (static_cast<uint32_t>(ch ^ (lane & 7)) << 4);
+          st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && r0 < p.S) {
+          tma_store_4d(&tm_o, stage, half * 64, r0, it.hh, it.bb);
+          tma_store_commit();
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      const int grow = q0 + q * kBlock + row;
+      const int grow = it.q0 + q * kBlock + row;
       if (p.lse != nullptr && grow < p.S)
-        p.lse[static_cast<size_t>(bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
+        p.lse[static_cast<size_t>(it.bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
+      gbase += it.n;
     }
+    if (lane == 0) tma_store_wait_read_all();
+    __syncwarp();
   } else if (warp < 12) {
     // ------------------------------------------------------------------ correction
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
@@ -676,34 +770,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
     bool ok = true;
-    for (int i = 1; i < n && ok; ++i) {
-      for (int q = 0; q < 2; ++q) {
-        {
-          // Stats for tile i are published after S_q(i) is full, which (tcgen05.commit
-          // tracks every earlier MMA of that Q tile) means PV_q(i-1) has finished writing O_q.
-          if (!wait_bar_warp(c, kBarStats + q, (i - 1) & 1, kRoleCorrection)) { ok = false; break; }
-          const float alpha = alpha_sm[q * kBlock + row];
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t o[32];
-              tmem_ld32_x32_sync(tO[q] + cc * 32, o);
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                float a0, a1;  // packed multiply: scalar FP32 math here would slow the MMAs
-                fma2(a0, a1, __uint_as_float(o[j]), __uint_as_float(o[j + 1]), alpha, alpha, 0.f, 0.f);
-                o[j] = __float_as_uint(a0);
-                o[j + 1] = __float_as_uint(a1);
-              }
-              tmem_st32_x32(tO[q] + cc * 32, o);
+    int sbase = 0;  // stats phases before this item
+    for (int r = 0; item_of(r) < p.num_items && ok; ++r) {
+      const Item it = item_at(item_of(r));
+      for (int i = 1; i < it.n && ok; ++i) {
+        for (int q = 0; q < 2; ++q) {
+          {
+            if (!wait_bar_warp(c, kBarStats + q, static_cast<uint32_t>((sbase + i - 1) & 1), kRoleCorrection)) {
+              ok = false;
+              break;
             }
-            tmem_wait_st();
+            const float alpha = alpha_sm[q * kBlock + row];
+            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t o[32];
+                tmem_ld32_x32_sync(tO[q] + cc * 32, o);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  float a0, a1;
+                  fma2(a0, a1, __uint_as_float(o[j]), __uint_as_float(o[j + 1]), alpha, alpha, 0.f, 0.f);
+                  o[j] = __float_as_uint(a0);
+                  o[j + 1] = __float_as_uint(a1);
+                }
+                tmem_st32_x32(tO[q] + cc * 32, o);
+              }
+              tmem_wait_st();
+            }
+            tc_fence_before();
           }
-          tc_fence_before();
+          warp_arrive(c, kBarOSafe + q, lane);
         }
-        warp_arrive(c, kBarOSafe + q, lane);
       }
+      sbase += it.n - 1;
     }
   }
 
@@ -730,6 +830,7 @@ std::once_flag g_encode_once;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported/failed
+int g_dev_sms[kMaxDevices];                 // SM count, set before the device is marked ready
 std::mutex g_dev_mutex;
 
 bool get_encoder() {
@@ -779,6 +880,12 @@ int prepare_device(int* dev_out) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  g_dev_sms[dev] = sms;
   g_dev_state[dev].store(1, std::memory_order_release);
   return ATTN_OK;
 }
@@ -897,12 +1004,16 @@ static int attn_launch(const void* q, const void* k, const void* v, void* o, flo
   prm.n_kv = static_cast<int>(n_kv);
   prm.n_qp = static_cast<int>(n_qp);
   prm.BH = static_cast<int>(BH);
+  prm.num_items = static_cast<int>(BH * n_qp);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 #ifdef ATTN_TEST_HOOKS
   prm.withhold = withhold;
 #endif
 
-  const dim3 grid(static_cast<unsigned>(BH * n_qp));
+  // One CTA per SM (the kernel holds all of an SM's tensor memory); each CTA walks its items.
+  const long long items = BH * n_qp;
+  const int sms = g_dev_sms[dev];
+  const dim3 grid(static_cast<unsigned>(items > sms ? sms : items));
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
   auto launch = [&](auto kernel) { kernel<<<grid, kThreads, kSmemBytes, st_>>>(tq, tk, tv, to, prm); };
   if (rebase_threshold_log2 == 8) {

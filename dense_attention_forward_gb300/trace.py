@@ -4,8 +4,8 @@
 
 builds libattn_trace.so if needed (the kernels of libattn.so with -DATTN_TRACE, see
 include/attn_trace.h), runs three warm-up launches, writes 256 MB to flush L2, runs one traced
-launch and prints one JSON line: the mean duration of each phase of a CTA, the gap between
-one CTA's exit and the next CTA's entry on the same SM, and the span of the launch. The
+launch and prints one JSON line: the mean duration of each phase of a CTA's first item, the
+rest of its items, the mean time per item, and the span of the launch. The
 numbers come from the GPU's nanosecond timer, so they include the stamps' own small cost;
 use them for where the time goes, not as the kernel's speed (bench.py measures that).
 """
@@ -64,20 +64,25 @@ def timeline(B: int, H: int, S: int, causal: bool = False, seed: int = 0) -> dic
     if call() != 0:
         raise RuntimeError("attn launch failed")
     torch.cuda.synchronize()
-    n = B * H * ((S + 255) // 256)
-    cap = min(n, 4096)
+    items = B * H * ((S + 255) // 256)
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    ctas = min(items, sms)  # one CTA per SM, each walking its share of the items
+    cap = min(ctas, 4096)
     buf = (ctypes.c_ulonglong * (8 * cap))()
     if lib.attn_trace_read(buf, cap) != 0:
         raise RuntimeError("attn_trace_read failed")
     t = np.frombuffer(buf, dtype=np.uint64).reshape(cap, 8).astype(np.int64)
-    return summarize(t, n, f"B={B} H={H} S={S} D=128" + (" causal" if causal else ""))
+    return summarize(t, items, ctas, f"B={B} H={H} S={S} D=128" + (" causal" if causal else ""))
 
 
-def summarize(t: np.ndarray, n: int, workload: str) -> dict:
+def summarize(t: np.ndarray, items: int, ctas: int, workload: str) -> dict:
     """Phase means (microseconds) of a [ctas, 8] array of trace words (layout in
-    include/attn_trace.h); n is the launch's CTA count."""
+    include/attn_trace.h): the first item of each CTA phase by phase, then the rest of its items
+    up to the final barrier, and the mean time per item. items is the launch's work-item count,
+    ctas its CTA count; the gap between one CTA's exit and the next CTA's entry on the same SM
+    is reported only where an SM ran several CTAs."""
     cap = t.shape[0]
-    ends = np.maximum(t[:, 3], t[:, 4])
+    first_end = np.maximum(t[:, 3], t[:, 4])
     gaps = []
     for sm in np.unique(t[:, 6]):
         sel = t[t[:, 6] == sm]
@@ -87,16 +92,19 @@ def summarize(t: np.ndarray, n: int, workload: str) -> dict:
     def mean_us(a):
         return round(float(np.mean(a)) / 1e3, 3)
 
+    per_cta = items / ctas
     return {
         "workload": workload,
-        "ctas": n, "ctas_traced": cap, "sms": int(len(np.unique(t[:, 6]))),
+        "items": items, "ctas": ctas, "ctas_traced": cap, "items_per_cta": round(per_cta, 3),
+        "sms": int(len(np.unique(t[:, 6]))),
         "span_us": round(float(t[:, 7].max() - t[:, 0].min()) / 1e3, 1),
         "cta_us": mean_us(t[:, 7] - t[:, 0]),
+        "per_item_us": mean_us((t[:, 5] - t[:, 0]) / per_cta),
         "setup_us": mean_us(t[:, 1] - t[:, 0]),
         "to_first_s_us": mean_us(t[:, 2] - t[:, 1]),
-        "kv_loop_us": mean_us(t[:, 3] - t[:, 2]),
+        "first_item_kv_loop_us": mean_us(t[:, 3] - t[:, 2]),
         "o0_to_o1_us": mean_us(t[:, 4] - t[:, 3]),
-        "to_final_barrier_us": mean_us(t[:, 5] - ends),
+        "later_items_us": mean_us(t[:, 5] - first_end),
         "final_barrier_to_exit_us": mean_us(t[:, 7] - t[:, 5]),
         "gap_between_ctas_us": round(float(np.mean(gaps)) / 1e3, 3) if gaps else None,
         "all_exited": bool(np.all(t[:, 7] > 0)),

@@ -184,7 +184,9 @@ const char* attn_status_string(int status);
  * ATTN_ERR_UNSUPPORTED_DEVICE / ATTN_ERR_LAUNCH if the word could not be read.
  *
  * Word layout: 0xA77E0000 | role << 8 | barrier, role 1 = TMA producer, 2 = MMA issue,
- * 3 = softmax, 4 = O correction; barrier = the index of the mbarrier whose wait ran out.
+ * 3 = softmax, 4 = O correction; barrier = the index of the mbarrier whose wait ran out
+ * (0-17), or 18 + q for the producer's wait on the count of Q tile q's S tiles that the
+ * softmax warps have taken.
  */
 int attn_device_status(unsigned int* word, int reset);
 

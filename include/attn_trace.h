@@ -4,10 +4,12 @@
  * point of attn.h is exported by the trace build too and behaves the same.
  *
  * The trace build records, for each CTA index below its capacity (4096 CTAs), eight 64-bit
- * words from the GPU's global nanosecond timer:
+ * words from the GPU's global nanosecond timer. A CTA walks several work items (pairs of Q
+ * tiles); words 2-4 belong to its first item:
  *   0 CTA entry, 1 setup done (barriers initialised, tensor memory allocated),
  *   2 Q tile 0's first S seen by the softmax, 3 O tile 0 complete, 4 O tile 1 complete,
- *   5 before the final CTA barrier, 6 the SM id (not a time), 7 CTA exit.
+ *   5 before the final CTA barrier (after the CTA's last item), 6 the SM id (not a time),
+ *   7 CTA exit.
  * A word is 0 if that point was not reached (or the CTA index is beyond the capacity).
  * Each launch overwrites the words of the CTAs it runs.
  */

@@ -9,14 +9,17 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("causal", [False, True])
 def test_trace_timeline(causal):
     from dense_attention_forward_gb300 import trace
-    d = trace.timeline(2, 8, 1024, causal=causal)
-    assert d["ctas"] == 2 * 8 * 4 and d["ctas_traced"] == d["ctas"]
-    assert d["all_exited"] and d["sms"] >= 1
-    for key in ("setup_us", "to_first_s_us", "kv_loop_us", "final_barrier_to_exit_us"):
+    # 2 x 8 heads x 16 items = 256 items: more than the SMs, so CTAs walk several items.
+    d = trace.timeline(2, 8, 4096, causal=causal)
+    assert d["items"] == 2 * 8 * 16 and d["ctas_traced"] == d["ctas"] <= d["items"]
+    assert d["items_per_cta"] > 1.0
+    assert d["all_exited"] and d["sms"] == d["ctas"]  # one CTA per SM
+    for key in ("setup_us", "to_first_s_us", "first_item_kv_loop_us", "later_items_us",
+                "final_barrier_to_exit_us", "per_item_us"):
         assert d[key] >= 0.0, (key, d)
-    assert d["to_first_s_us"] > 0.0 and d["kv_loop_us"] > 0.0
+    assert d["to_first_s_us"] > 0.0 and d["first_item_kv_loop_us"] > 0.0 and d["later_items_us"] > 0.0
     assert d["cta_us"] <= d["span_us"] + 1e-3
-    assert d["cta_us"] >= d["setup_us"] + d["to_first_s_us"] + d["kv_loop_us"] - 1e-3
+    assert d["cta_us"] >= d["setup_us"] + d["to_first_s_us"] + d["first_item_kv_loop_us"] - 1e-3
 
 
 def test_trace_build_matches_product():

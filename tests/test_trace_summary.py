@@ -1,25 +1,34 @@
-"""The timeline tool's host arithmetic on a synthetic trace (CPU): phase means and the gap
-between one CTA's exit and the next CTA's entry on the same SM."""
+"""The timeline tool's host arithmetic on a synthetic trace (CPU): phase means of the first
+item, the time per item, and the gap between CTAs that share an SM."""
 import numpy as np
 
 from dense_attention_forward_gb300.trace import summarize
 
 
 def test_summarize_synthetic_trace():
-    # words: entry, setup, first S, O0 full, O1 full, before final barrier, SM id, exit (ns)
+    # words: entry, setup, first S, O0 full, O1 full (first item), before final barrier, SM id,
+    # exit (ns). Two CTAs on two SMs, 4 items: 2 per CTA.
+    t = np.array([
+        [0, 200, 2200, 50000, 50800, 101000, 0, 102000],
+        [0, 300, 2300, 50100, 50900, 101200, 1, 102100],
+    ], dtype=np.int64)
+    d = summarize(t, 4, 2, "synthetic")
+    assert d["items"] == 4 and d["ctas"] == 2 and d["ctas_traced"] == 2 and d["sms"] == 2
+    assert d["items_per_cta"] == 2.0
+    assert d["setup_us"] == 0.25 and d["to_first_s_us"] == 2.0
+    assert d["first_item_kv_loop_us"] == 47.8
+    assert d["o0_to_o1_us"] == 0.8
+    assert d["later_items_us"] == 50.25          # from the later of O0 / O1 full to the final barrier
+    assert d["per_item_us"] == 50.55             # (101000 + 101200) / 2 / 2 ns
+    assert d["final_barrier_to_exit_us"] == 0.95
+    assert d["gap_between_ctas_us"] is None      # one CTA per SM
+    assert d["span_us"] == 102.1 and d["all_exited"]
+
+
+def test_summarize_gap_between_ctas_on_one_sm():
     t = np.array([
         [0, 200, 2200, 50000, 50800, 51000, 0, 52000],
-        [0, 300, 2300, 50100, 50900, 51200, 1, 52100],
-        [52800, 53000, 55000, 103000, 103800, 104000, 0, 105000],    # next CTA on SM 0: gap 800
-        [53100, 53300, 55300, 103300, 104100, 104300, 1, 105300],    # next CTA on SM 1: gap 1000
+        [52800, 53000, 55000, 103000, 103800, 104000, 0, 105000],   # next CTA on SM 0: gap 800
     ], dtype=np.int64)
-    d = summarize(t, 4, "synthetic")
-    assert d["ctas"] == 4 and d["ctas_traced"] == 4 and d["sms"] == 2
-    assert d["setup_us"] == 0.225 and d["to_first_s_us"] == 2.0   # (200 + 300 + 200 + 200) / 4 ns
-    assert d["kv_loop_us"] == 47.9        # (47800 + 47800 + 48000 + 48000) / 4 ns
-    assert d["o0_to_o1_us"] == 0.8
-    assert d["to_final_barrier_us"] == 0.225   # from the later of O0 / O1 full
-    assert d["final_barrier_to_exit_us"] == 0.975
-    assert d["gap_between_ctas_us"] == 0.9
-    assert d["span_us"] == 105.3 and d["all_exited"]
-    assert d["cta_us"] == 52.125
+    d = summarize(t, 2, 2, "synthetic")
+    assert d["gap_between_ctas_us"] == 0.8 and d["items_per_cta"] == 1.0
