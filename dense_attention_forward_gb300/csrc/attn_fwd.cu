@@ -11,9 +11,10 @@
 //    epilogue instead of a CTA exit, launch and pipeline fill per item.
 //  * Loads (Ch. 3, Ch. 6): Q0, K0 and Q1 leave right after the barriers are initialised; one
 //    TMA warp then streams K and V as separate tokens through a kStages-slot ring of 32 KB
-//    SW128 slots; a slot is refilled once the second Q tile's S-full commit that follows its
-//    last consumer (that tile's QK for K, its PV for V) has arrived, so no MMA commit is spent
-//    on freeing slots.
+//    SW128 slots. A slot is refilled once the second Q tile's softmax warps have taken the S
+//    that follows its last consumer (that tile's QK for K, its PV for V): they publish a
+//    monotonic count of the S tiles they have taken, so no MMA commit is spent on freeing
+//    slots and no parity wait can mistake one phase for another two steps away.
 //  * MMA (Ch. 1 §A/§C, Ch. 2, Ch. 5, Ch. 7, Ch. 13): tcgen05.mma M128 N128 K16, S_q = Q_q K^T
 //    (both K-major SW128 in shared memory) and O_q += P_q V (P from tensor memory, V MN-major
 //    SW128). One warp per Q tile issues that tile's MMAs: in K/V tile i, the PV_q(i) steps of
@@ -30,15 +31,17 @@
 //    in other warps slows the tensor pipe.
 //  * Correction (Ch. 11, Ch. 12): 4 warps shared by both Q tiles rescale O in tensor memory
 //    when any row of their 32 rebased.
-//  * Epilogue (Ch. 1): each softmax warp turns its 32 rows of O / l into BF16, stages them
-//    SW128 in the dead Q_q buffer and TMA-stores them (32-row boxes, no cross-warp barrier);
-//    lse = (m + log2 l) * ln 2 is written by the same threads.
+//  * Epilogue (Ch. 1): each softmax warp reads its 32 rows of O out of tensor memory (which
+//    frees O_q for the next item's first PV), turns O / l into BF16 and TMA-stores it from its
+//    own 4 KB SW128 staging slice in two half-width passes (32-row boxes, no cross-warp
+//    barrier); lse = (m + log2 l) * ln 2 is written by the same threads.
 //
 // Barrier phases count across the items of a CTA: per K/V tile of the CTA's stream (S full,
 // O safe, the turns, the P parts), per item (Q full, O full) or per token (the K/V ring).
 // TMEM: 512 columns = S0 [0,128) | S1 [128,256) | O0 [256,384) | O1 [384,512); P_q occupies
 // the first 64 columns of S_q. Warps 0-7 softmax, 8-11 correction, 12 and 13 MMA issue (13
-// also owns the TMEM allocation), 14 loads. Every mbarrier wait is bounded (about two
+// also owns the TMEM allocation), 14 loads, 15 set-up (then idle, so that no working warp runs
+// diverged set-up code). Every mbarrier wait is bounded (about two
 // seconds); a CTA that gives up records the failure in a device status word, drains its own
 // TMA loads and MMAs, frees its tensor memory and exits. The only other barriers are the
 // CTA-wide ones at entry and exit, and the named barriers on which each Q tile's softmax warps
@@ -78,6 +81,7 @@ constexpr int kLoadWarp = 14;                    // TMA producer
 constexpr int kIssueWarp0 = 12;                  // MMA issue for Q tile 0
 constexpr int kIssueWarp1 = 13;                  // MMA issue for Q tile 1; also owns the TMEM allocation
 constexpr int kTmemWarp = kIssueWarp1;
+constexpr int kSetupWarp = 15;                   // set-up (barriers, first loads); idle after
 // P_q(i) is stored and consumed in parts: packed BF16 pairs (TMEM columns) [kPCut[k], kPCut[k+1]).
 // A PV K16 step reads 8 of them, so every cut is a multiple of 8. A small first part lets the
 // tensor pipe start PV_q(i) early; QK_q(i+1) waits for the last part.
@@ -344,6 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   struct Item {
     int qp, bh, hh, bb, q0, n;
   };
+  // Items of this CTA: rounds r < n_mine (the rounds that exist form a prefix; the last, partial
+  // round reaches the CTAs at positions below its size).
+  const int full_rounds = p.num_items / stride;
+  const int last_pos = (kCausal && (full_rounds & 1)) ? stride - 1 - item0 : item0;
+  const int n_mine = full_rounds + (last_pos < p.num_items % stride ? 1 : 0);
   auto item_at = [&](int it) {
     Item r;
     if constexpr (kCausal) {
@@ -390,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_4d_hint(dst + kSliceBytes, map, bar, 64, row, it.hh, it.bb, policy);
   };
 
-  if (threadIdx.x == 0) {
+  // Set-up runs in a warp with no later role, so that no working warp ever runs diverged code.
+  if (warp == kSetupWarp && lane == 0) {
     mbar_init(c.bar(kBarQFull + 0), 1);
     mbar_init(c.bar(kBarQFull + 1), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(c.bar(kBarKVFull + s), 1);
@@ -452,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 1;           // global token 0 (the first item's K0) was loaded at set-up
       int gbase = 0;            // global index of the item's first K/V tile
       int q_loads[2] = {1, 1};  // Q tile loads so far (the phases of the Q barriers)
-      for (int k = 0; item_of(k) < p.num_items && ok; ++k) {
+      for (int k = 0; k < n_mine && ok; ++k) {
         const Item it = item_at(item_of(k));
         for (int u = 0; u < 2 * it.n; ++u) {
           const int T = 2 * gbase + u;
@@ -537,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile within the current item, n its tile count.
     int k = 0;
     int n = kCausal ? item_at(item_of(0)).n : p.n_kv;
-    bool next_item = item_of(1) < p.num_items;
+    bool next_item = 1 < n_mine;
     for (int gt = 0, i = 0; ok; ++gt) {
       const int tv = 2 * gt + 1, tk = 2 * gt + 2;
       const bool more = i + 1 < n;
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!next_item) break;
         i = 0;
         n = kCausal ? item_at(item_of(k)).n : p.n_kv;
-        next_item = item_of(k + 1) < p.num_items;
+        next_item = k + 1 < n_mine;
       }
     }
     if (!ok && lane == 0) {
@@ -620,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = base + kOffStage + (q * 4 + (warp & 3)) * kStageWarpBytes;
     bool ok = true;
     int gbase = 0, k = 0;
-    for (; item_of(k) < p.num_items && ok; ++k) {
+    for (; k < n_mine && ok; ++k) {
       const Item it = item_at(item_of(k));
-      const bool next_item = item_of(k + 1) < p.num_items;
+      const bool next_item = k + 1 < n_mine;
       float m_kept = -INFINITY;
       float l = 0.f;
       float lf = 0.f;
@@ -771,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO[2] = {tmem + lane_field + 256u, tmem + lane_field + 384u};
     bool ok = true;
     int sbase = 0;  // stats phases before this item
-    for (int r = 0; item_of(r) < p.num_items && ok; ++r) {
+    for (int r = 0; r < n_mine && ok; ++r) {
       const Item it = item_at(item_of(r));
       for (int i = 1; i < it.n && ok; ++i) {
         for (int q = 0; q < 2; ++q) {
