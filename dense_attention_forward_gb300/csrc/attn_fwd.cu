@@ -118,7 +118,9 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffFail = kOffAbort + 4;                    // int[2]: issuing warp q has stopped issuing
 constexpr int kOffSeen = kOffFail + 8;                     // int[2]: S_q tiles seen by the softmax warps
 constexpr int kOffAlpha = (kOffSeen + 8 + 15) & ~15;       // float[2][128]
-constexpr int kSmemUsed = kOffAlpha + 2 * kBlock * 4;
+constexpr int kMaxOrder = 384;                             // causal: most items a CTA sorts
+constexpr int kOffOrder = kOffAlpha + 2 * kBlock * 4;      // uint16[kMaxOrder]: the CTA's causal item order
+constexpr int kSmemUsed = kOffOrder + kMaxOrder * 2;
 constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for the 1024-byte alignment
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -322,7 +324,7 @@ __device__ __forceinline__ void static_for(F&& f) {
 // tiles 2qp and 2qp+1 walks K/V tiles 0..2qp+1 only; its diagonal tiles are masked per
 // element, and Q tile 2qp runs tile 2qp+1 fully masked (P = 0) so both Q tiles keep the same
 // K/V schedule. Items are dealt to the CTAs longest first in a snake order, which evens out
-// the CTAs' totals of K/V tiles.
+// the CTAs' totals of K/V tiles; each CTA then takes its items head by head (see sorted_order).
 template <int kThr, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rounds r = 0, 1, ...: dense, item r * gridDim.x + c (items are numbered head-major, so the
   // CTAs of one round share K/V in L2); causal, items sorted longest first across all heads and
   // dealt out in a snake (c, then 2 * gridDim.x - 1 - c, ...) so that every CTA gets a similar
-  // total of K/V tiles.
+  // total of K/V tiles (the CTA then takes its own items in head order, see sorted_order).
   const int item0 = static_cast<int>(blockIdx.x);
   const int stride = static_cast<int>(gridDim.x);
   auto item_of = [&](int r) {
@@ -369,6 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     return r;
   };
 
+  // Causal: the snake sets which items a CTA holds (and so the balance); the CTA takes them by
+  // (batch * head, longest first), so that at any moment the CTAs work on few heads and their
+  // K/V tiles are read from DRAM about once instead of once per round. The order is sorted at
+  // set-up into shared memory by the set-up warp; a CTA with more than kMaxOrder items keeps
+  // the round order. sort_key packs (batch * head, item) into one 64-bit key.
+  uint16_t* const order_sm = reinterpret_cast<uint16_t*>(smem + kOffOrder);
+  const bool sorted_order = kCausal && n_mine <= kMaxOrder;
+  auto sort_key = [&](int r) {
+    const uint32_t it = static_cast<uint32_t>(item_of(r));
+    return (static_cast<unsigned long long>(it % static_cast<uint32_t>(p.BH)) << 32) | it;
+  };
+  auto mine = [&](int k) { return item_of(sorted_order ? static_cast<int>(order_sm[k]) : k); };
   if (threadIdx.x == 0) {
     ATTN_STAMP(0);
     ATTN_STAMP_SM();
@@ -400,6 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Set-up runs in a warp with no later role, so that no working warp ever runs diverged code.
+  // With a sorted order it first finds the CTA's first item (the smallest key, a warp-wide
+  // minimum), so that the first loads leave before the rest of the order is sorted.
+  int r_first = 0;
+  if (warp == kSetupWarp && sorted_order) {
+    unsigned long long* const keys = reinterpret_cast<unsigned long long*>(smem + kOffStage);
+    unsigned long long best = ~0ull;
+    for (int r = lane; r < n_mine; r += 32) {
+      keys[r] = sort_key(r);
+      best = keys[r] < best ? keys[r] : best;
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o < best ? o : best;
+    }
+    r_first = -1;
+    for (int r = lane; r < n_mine; r += 32)
+      if (keys[r] == best) r_first = r;
+    for (int off = 16; off > 0; off >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, r_first, off);
+      r_first = o > r_first ? o : r_first;
+    }
+    __syncwarp();
+  }
   if (warp == kSetupWarp && lane == 0) {
     mbar_init(c.bar(kBarQFull + 0), 1);
     mbar_init(c.bar(kBarQFull + 1), 1);
@@ -423,11 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
-    const Item it = item_at(item_of(0));
+    const Item it = item_at(item_of(r_first));
     const uint64_t once = l2_policy_evict_first();
     load_q(it, 0, once);
     if (!ATTN_WITHHELD(p, 0)) load_token(it, 0, 0, l2_policy_evict_last());
     load_q(it, 1, once);
+  }
+  if (warp == kSetupWarp && sorted_order) {
+    // Rank sort of the keys staged above in the O staging area (unused until the first epilogue).
+    const unsigned long long* const keys = reinterpret_cast<const unsigned long long*>(smem + kOffStage);
+    __syncwarp();
+    for (int r = lane; r < n_mine; r += 32) {
+      const unsigned long long kr = keys[r];
+      int rank = 0;
+      for (int r2 = 0; r2 < n_mine; ++r2) rank += keys[r2] < kr ? 1 : 0;
+      order_sm[rank] = static_cast<uint16_t>(r);
+    }
+    __syncwarp();
   }
   if (warp == kTmemWarp) {
     tmem_alloc(base + kOffTmemSlot, 512);
@@ -463,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gbase = 0;            // global index of the item's first K/V tile
       int q_loads[2] = {1, 1};  // Q tile loads so far (the phases of the Q barriers)
       for (int k = 0; k < n_mine && ok; ++k) {
-        const Item it = item_at(item_of(k));
+        const Item it = item_at(mine(k));
         for (int u = 0; u < 2 * it.n; ++u) {
           const int T = 2 * gbase + u;
           if (T == 0) continue;
@@ -546,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One flat loop over the CTA's stream of K/V tiles: gt counts tiles across items, i is the
     // tile within the current item, n its tile count.
     int k = 0;
-    int n = kCausal ? item_at(item_of(0)).n : p.n_kv;
+    int n = kCausal ? item_at(mine(0)).n : p.n_kv;
     bool next_item = 1 < n_mine;
     for (int gt = 0, i = 0; ok; ++gt) {
       const int tv = 2 * gt + 1, tk = 2 * gt + 2;
@@ -602,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++k;
         if (!next_item) break;
         i = 0;
-        n = kCausal ? item_at(item_of(k)).n : p.n_kv;
+        n = kCausal ? item_at(mine(k)).n : p.n_kv;
         next_item = k + 1 < n_mine;
       }
     }
@@ -631,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int gbase = 0, k = 0;
     for (; k < n_mine && ok; ++k) {
-      const Item it = item_at(item_of(k));
+      const Item it = item_at(mine(k));
       const bool next_item = k + 1 < n_mine;
       float m_kept = -INFINITY;
       float l = 0.f;
@@ -782,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int sbase = 0;  // stats phases before this item
     for (int r = 0; r < n_mine && ok; ++r) {
-      const Item it = item_at(item_of(r));
+      const Item it = item_at(mine(r));
       for (int i = 1; i < it.n && ok; ++i) {
         for (int q = 0; q < 2; ++q) {
           {
