@@ -53,6 +53,10 @@ typedef enum {
  *   stream  : a cudaStream_t (NULL = the legacy default stream). The call is asynchronous:
  *             it enqueues one kernel and returns; nothing is synchronised on the host.
  *
+ * Resources: the kernel launches min(B*H*ceil(S/256), number of SMs) CTAs of 512 threads, each
+ * holding one SM's tensor memory and ~227 KB of its shared memory, and each working through
+ * its share of the work items (256 query rows of one (b, h) against all of that head's keys).
+ *
  * Ownership: all buffers belong to the caller. The library allocates no device memory and
  * keeps no per-call state; it caches only per-device launch attributes.
  *
