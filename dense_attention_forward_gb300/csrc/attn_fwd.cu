@@ -133,13 +133,18 @@ __device__ unsigned int g_attn_status = 0;
 
 // Optional timeline trace (built only into libattn_trace.so, with -DATTN_TRACE): per CTA, the
 // globaltimer at entry (0), after setup (1), when Q tile 0's first S is seen (2), when O_0 and
-// O_1 are full (3, 4), before the final barrier (5), the SM id (6) and at exit (7). In the
-// ordinary build the stamps compile to nothing.
+// O_1 are full (3, 4), before the final barrier (5), the SM id (6) and at exit (7); and, at the
+// boundary between the CTA's first two items, for Q tile 0: the first item's last S seen (8),
+// its last P part stored (9), O read out of tensor memory (10), epilogue done (11), the next
+// item's first S seen (12) and first P part stored (13), and by the issuing warp the next
+// item's first QK issued (14) and first PV issued (15). In the ordinary build the stamps
+// compile to nothing.
 #ifdef ATTN_TRACE
 #ifndef ATTN_TRACE_CTAS
 #define ATTN_TRACE_CTAS 4096
 #endif
-__device__ unsigned long long g_attn_trace[ATTN_TRACE_CTAS * 8];
+constexpr int kTraceWords = 16;  // per CTA
+__device__ unsigned long long g_attn_trace[ATTN_TRACE_CTAS * kTraceWords];
 __device__ __forceinline__ unsigned sm_id() {
   unsigned r;
   asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
@@ -147,13 +152,19 @@ __device__ __forceinline__ unsigned sm_id() {
 }
 #define ATTN_STAMP(k)                                                                        \
   do {                                                                                       \
-    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * 8u + (k)] = global_timer_ns(); \
+    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * kTraceWords + (k)] = global_timer_ns(); \
   } while (0)
 #define ATTN_STAMP_SM()                                                   \
   do {                                                                    \
-    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * 8u + 6] = sm_id(); \
+    if (blockIdx.x < ATTN_TRACE_CTAS) g_attn_trace[blockIdx.x * kTraceWords + 6] = sm_id(); \
+  } while (0)
+// A stamp taken only when cond holds; outside the trace build neither is compiled.
+#define ATTN_STAMP_IF(cond, k) \
+  do {                          \
+    if (cond) ATTN_STAMP(k);    \
   } while (0)
 #else
+#define ATTN_STAMP_IF(cond, k)
 #define ATTN_STAMP(k) \
   do {                \
   } while (0)
@@ -620,6 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             tc_fence_after();
             issue_pv(static_cast<uint32_t>(tv % kStages), c0 / 8, c1 / 8, pi == 0 && i == 0);
+            ATTN_STAMP_IF(q == 0 && k == 1 && pi == 0 && i == 0, 15);
             if constexpr (pi == kPParts - 1) {
               if (more) {
                 issue_qk(static_cast<uint32_t>(tk % kStages), true);
@@ -633,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_qk(static_cast<uint32_t>(tk % kStages), true);
                     mma_commit(c.bar(kBarSFull + q));
+                    ATTN_STAMP_IF(q == 0 && k == 0, 14);
                   }
                 } else if (q == 0) {
                   tc_fence_before();
@@ -692,6 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if ((warp & 3) == 0 && lane == 0) st_release_shared(s_seen + q, gt + 1);
+        ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 0 && i == it.n - 1, 8);
+        ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 1 && i == 0, 12);
         if (gt == 0 && warp == 0 && lane == 0) ATTN_STAMP(2);
         tc_fence_after();
         uint32_t sr[128];
@@ -763,6 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
           named_bar_arrive(kBarP + 2 * pi + q, 160);
+          ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 0 && pi == kPParts - 1 && i == it.n - 1, 9);
+          ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 1 && pi == 0 && i == 0, 13);
         };
         static_for<kPParts>(part);
         lf += (lf0 + lf1) + (lf2 + lf3);
@@ -788,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         warp_arrive(c, kBarOSafe + q, lane);  // O_q drained
       }
+      ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 0, 10);
       const int r0 = it.q0 + q * kBlock + (warp & 3) * 32;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -818,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grow = it.q0 + q * kBlock + row;
       if (p.lse != nullptr && grow < p.S)
         p.lse[static_cast<size_t>(it.bh) * p.S + grow] = (m_kept + log2f(lf)) * 0.69314718055994531f;
+      ATTN_STAMP_IF(warp == 0 && lane == 0 && k == 0, 11);
       gbase += it.n;
     }
     if (lane == 0) tma_store_wait_read_all();
@@ -1202,7 +1221,7 @@ int attn_version(void) { return (1 << 16) | 0; }
 int attn_trace_read(unsigned long long* out, int max_ctas) {
   if (!out || max_ctas <= 0) return ATTN_ERR_INVALID_ARG;
   const int nct = max_ctas < ATTN_TRACE_CTAS ? max_ctas : ATTN_TRACE_CTAS;
-  if (cudaMemcpyFromSymbol(out, gb300::g_attn_trace, static_cast<size_t>(nct) * 8 * sizeof(unsigned long long)) !=
+  if (cudaMemcpyFromSymbol(out, gb300::g_attn_trace, static_cast<size_t>(nct) * gb300::kTraceWords * sizeof(unsigned long long)) !=
       cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -1211,7 +1230,7 @@ int attn_trace_read(unsigned long long* out, int max_ctas) {
 }
 
 int attn_trace_clear(void) {
-  static unsigned long long zero[ATTN_TRACE_CTAS * 8];
+  static unsigned long long zero[ATTN_TRACE_CTAS * gb300::kTraceWords];
   if (cudaMemcpyToSymbol(gb300::g_attn_trace, zero, sizeof(zero)) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;

@@ -21,6 +21,7 @@ import numpy as np
 from . import build as _build
 
 _trace_lib = None
+WORDS = 16  # trace words per CTA
 
 _ARGS = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_void_p]
 
@@ -68,19 +69,26 @@ def timeline(B: int, H: int, S: int, causal: bool = False, seed: int = 0) -> dic
     sms = torch.cuda.get_device_properties(q.device).multi_processor_count
     ctas = min(items, sms)  # one CTA per SM, each walking its share of the items
     cap = min(ctas, 4096)
-    buf = (ctypes.c_ulonglong * (8 * cap))()
+    buf = (ctypes.c_ulonglong * (WORDS * cap))()
     if lib.attn_trace_read(buf, cap) != 0:
         raise RuntimeError("attn_trace_read failed")
-    t = np.frombuffer(buf, dtype=np.uint64).reshape(cap, 8).astype(np.int64)
+    t = np.frombuffer(buf, dtype=np.uint64).reshape(cap, WORDS).astype(np.int64)
     return summarize(t, items, ctas, f"B={B} H={H} S={S} D=128" + (" causal" if causal else ""))
 
 
+BOUNDARY = {  # word -> name, times relative to word 8 (the first item's last S seen)
+    9: "last_p_stored", 3: "o_full", 10: "o_read", 11: "epilogue_done",
+    14: "next_qk_issued", 12: "next_s_seen", 13: "next_p_stored", 15: "next_pv_issued",
+}
+
+
 def summarize(t: np.ndarray, items: int, ctas: int, workload: str) -> dict:
-    """Phase means (microseconds) of a [ctas, 8] array of trace words (layout in
+    """Phase means (microseconds) of a [ctas, 16] array of trace words (layout in
     include/attn_trace.h): the first item of each CTA phase by phase, then the rest of its items
     up to the final barrier, and the mean time per item. items is the launch's work-item count,
     ctas its CTA count; the gap between one CTA's exit and the next CTA's entry on the same SM
-    is reported only where an SM ran several CTAs."""
+    is reported only where an SM ran several CTAs. "boundary" gives the medians, over the CTAs
+    with a second item, of the boundary stamps (Q tile 0) after the first item's last S."""
     cap = t.shape[0]
     first_end = np.maximum(t[:, 3], t[:, 4])
     gaps = []
@@ -93,6 +101,12 @@ def summarize(t: np.ndarray, items: int, ctas: int, workload: str) -> dict:
         return round(float(np.mean(a)) / 1e3, 3)
 
     per_cta = items / ctas
+    two = t[(t[:, 12] > 0) & (t[:, 8] > 0)]
+    boundary = None
+    if len(two):
+        boundary = {"ctas": int(len(two))}
+        for w, name in BOUNDARY.items():
+            boundary[name + "_us"] = round(float(np.median(two[:, w] - two[:, 8])) / 1e3, 3)
     return {
         "workload": workload,
         "items": items, "ctas": ctas, "ctas_traced": cap, "items_per_cta": round(per_cta, 3),
@@ -108,6 +122,7 @@ def summarize(t: np.ndarray, items: int, ctas: int, workload: str) -> dict:
         "final_barrier_to_exit_us": mean_us(t[:, 7] - t[:, 5]),
         "gap_between_ctas_us": round(float(np.mean(gaps)) / 1e3, 3) if gaps else None,
         "all_exited": bool(np.all(t[:, 7] > 0)),
+        "boundary": boundary,
     }
 
 

@@ -20,6 +20,14 @@ def test_trace_timeline(causal):
     assert d["to_first_s_us"] > 0.0 and d["first_item_kv_loop_us"] > 0.0 and d["later_items_us"] > 0.0
     assert d["cta_us"] <= d["span_us"] + 1e-3
     assert d["cta_us"] >= d["setup_us"] + d["to_first_s_us"] + d["first_item_kv_loop_us"] - 1e-3
+    # The boundary between a CTA's first two items, in the order the protocol imposes.
+    b = d["boundary"]
+    assert b is not None and b["ctas"] >= 1
+    # (stamps of one thread are ordered; the issuing warp's may pass the softmax warp's own
+    # stamp of a barrier arrival, so only S seen orders the next PV)
+    assert 0 < b["last_p_stored_us"] <= b["o_full_us"] <= b["o_read_us"] <= b["epilogue_done_us"]
+    assert b["epilogue_done_us"] <= b["next_s_seen_us"] <= b["next_p_stored_us"]
+    assert b["next_qk_issued_us"] <= b["next_s_seen_us"] <= b["next_pv_issued_us"]
 
 
 def test_trace_build_matches_product():
@@ -42,7 +50,7 @@ def test_trace_build_matches_product():
     assert st == 0
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    buf = (ctypes.c_ulonglong * 8)()
+    buf = (ctypes.c_ulonglong * trace.WORDS)()
     assert lib.attn_trace_read(buf, 1) == 0
     t = np.frombuffer(buf, dtype=np.uint64).astype(np.int64)
     assert t[0] <= t[1] <= t[2] <= max(t[3], t[4]) <= t[5] <= t[7]
