@@ -35,9 +35,9 @@ L2_FLUSH_BYTES = 256 << 20
 # keyed by sweep entry; each is valid only for the kernel source it was taken on (hash of the
 # kernel's CUDA sources), and is reported as null otherwise.
 TRAFFIC: dict[str, tuple[int, str]] = {
-    "s4k": (240313600, "1c35245e9780a816"),         # 201,399,040 B read + 38,914,560 B written
-    "s16k": (247014400, "1c35245e9780a816"),        # 201,966,592 B read + 45,047,808 B written
-    "s4k_causal": (282098688, "1c35245e9780a816"),  # 236,579,584 B read + 45,519,104 B written
+    "s4k": (240544768, "a8b815de643e88de"),         # 201,434,368 B read + 39,110,400 B written
+    "s16k": (244620288, "a8b815de643e88de"),        # 201,450,752 B read + 43,169,536 B written
+    "s4k_causal": (282608128, "a8b815de643e88de"),  # 237,624,064 B read + 44,984,064 B written
 }
 
 # Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64

@@ -655,9 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       };
       static_for<kPParts>(part);
+      // Lanes 1-31 only wait at the named barriers; they need lane 0's result for the loop test.
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (more) {
         ++i;
       } else {
