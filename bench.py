@@ -40,6 +40,8 @@ TRAFFIC: dict[str, tuple[int, str]] = {
     "s4k_causal": (282608128, "a8b815de643e88de"),  # 237,624,064 B read + 44,984,064 B written
     "s8k": (242760192, "a8b815de643e88de"),         # 201,384,192 B read + 41,376,000 B written
     "ragged": (843931392, "a8b815de643e88de"),      # 648,556,544 B read + 195,374,848 B written
+    "s8k_causal": (280591616, "a8b815de643e88de"),  # 234,008,832 B read + 46,582,784 B written
+    "s16k_causal": (337310208, "a8b815de643e88de"), # 292,638,208 B read + 44,672,000 B written
 }
 
 # Dense BF16 tensor rate of one SM: an M128 N128 K16 tcgen05.mma (2*128*128*16 FLOP) every 64
